@@ -1,0 +1,171 @@
+/*
+ * convrot.h -- C ABI of the ConvRot W4A8 linear layer for GB300 (sm_103a).
+ *
+ * The layer (ComfyUI Turing Utils page on comfy.icu, node list, entry "Load
+ * ConvRot DiT and Load ConvRot CLIP also accept ComfyUI-native nvfp4 layers")
+ * keeps its weights in NVFP4, applies the same 256-point block rotation
+ * ("paired ConvRot256") to the activations and to the decoded weights,
+ * quantises both to row-scaled S8 and multiplies them with an integer GEMM
+ * whose epilogue dequantises to BF16 / FP16 / FP32:
+ *
+ *     y[m, n] = s_a[m] * s_w[n] * sum_k q_a[m, k] * q_w[n, k]
+ *
+ * Three calls make one layer: convrot_prepare_weight (NVFP4 decode + FP32
+ * rotation + S8 quantisation of the weight rows), convrot_quant_act
+ * ((SwiGLU +) FP32 rotation + S8 quantisation of the token rows) and
+ * convrot_gemm (integer GEMM + dequant epilogue).
+ *
+ * Conventions shared by every call:
+ *   - Every pointer is a DEVICE pointer owned by the caller; nothing is
+ *     allocated, freed or retained by the library.
+ *   - Work is enqueued on `stream` (0 = legacy default stream) and the call
+ *     returns without synchronising.  Outputs are valid once the stream has
+ *     reached the work.
+ *   - Matrices are row-major.  Leading dimensions (ld_*) count ELEMENTS of
+ *     the matrix's own storage type.
+ *   - K is the logical reduction width; K_p = convrot_padded_k(K) is K
+ *     rounded up to a multiple of 256 (both operands are zero-padded before
+ *     the rotation).  K_p <= CONVROT_MAX_KP.
+ *   - M == 0 or N == 0 is a valid empty call (nothing is launched).
+ *   - Return value: CONVROT_OK or one of the error codes below.  A failing
+ *     call launches nothing and leaves the outputs untouched.  No call
+ *     aborts or throws.
+ *
+ * S8 code storage.  The rotated operands are quantised to integer codes in
+ * [-127, 127].  They can be written either as int8 (CONVROT_CODES_S8, one
+ * byte per code) or as FP16 values holding the same integers exactly
+ * (CONVROT_CODES_F16, two bytes per code).  convrot_gemm reads the FP16
+ * form: sm_103a tensor cores have no 8-bit integer MMA, so the GEMM runs the
+ * FP16 tensor-core path, whose FP32 accumulation of these integer products
+ * is exact, and it converts to int32 every 512 K.  The int32 accumulator is
+ * therefore bit-exact.
+ */
+#ifndef CONVROT_H
+#define CONVROT_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CONVROT_BLOCK 256          /* rotation block (ConvRot256)           */
+#define CONVROT_MAX_KP 65536       /* largest padded K accepted             */
+
+typedef enum {
+    CONVROT_OK = 0,
+    CONVROT_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld too small, ... */
+    CONVROT_ERR_MISALIGNED = 2,    /* a pointer / pitch breaks an alignment rule     */
+    CONVROT_ERR_UNSUPPORTED = 3,   /* dtype / code format / K_p beyond the limit     */
+    CONVROT_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed           */
+    CONVROT_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up waiting (see convrot_device_error) */
+} convrot_status;
+
+typedef enum { CONVROT_BF16 = 0, CONVROT_FP16 = 1, CONVROT_FP32 = 2 } convrot_dtype;
+
+typedef enum { CONVROT_CODES_S8 = 0, CONVROT_CODES_F16 = 1 } convrot_codes;
+
+/* K rounded up to a multiple of CONVROT_BLOCK; 0 for K <= 0. */
+int convrot_padded_k(int K);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* convrot_status_string(int status);
+
+/*
+ * Weight preparation: NVFP4 decode + ConvRot256 rotation in FP32 + row-scaled
+ * S8 quantisation (the page's "NVFP4 decode, FP32 weight rotation and S8
+ * quantization are fused"; the stored NVFP4 bytes are only read).
+ *
+ *   w_fp4   [N][K_s/2] uint8, K_s = ceil(K/16)*16, rows contiguous.  Byte j of
+ *           a row holds element 2j in its low nibble, 2j+1 in its high nibble;
+ *           each nibble is an E2M1 code (sign bit 3).  Elements K..K_s-1 are
+ *           serialised padding and are ignored whatever they hold.
+ *   w_sf    [N][K_s/16] uint8 E4M3 ("FN") block scales, row-major.
+ *   w_tensor_scale  one FP32 (device memory): the NVFP4 tensor scale t.
+ *   w_q     [N][ld_wq] codes in `fmt`, columns 0..K_p-1 written (the zero
+ *           padding included); ld_wq >= K_p.
+ *   w_scale [N] FP32 row scales s_w (0 for a degenerate row).
+ *
+ * Decoded weight w = E2M1 * E4M3 * t.  Per row: r = rotate(w padded to K_p);
+ * s_w = fp32(max|r| / 127); q = clamp(rint(r * fp32(1/s_w)), -127, 127), the
+ * product and rounding done in FP32 (half to even).  A row whose s_w is 0 or
+ * whose reciprocal overflows is written as all-zero codes with s_w = 0.
+ * Alignment: w_fp4 8-byte aligned; F16 codes: w_q 2-byte aligned.
+ */
+int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
+                           const float* w_tensor_scale, int N, int K,
+                           void* w_q, convrot_codes fmt, int64_t ld_wq,
+                           float* w_scale, cudaStream_t stream);
+
+/*
+ * Activation quantisation: optional SwiGLU prologue, then ConvRot256 rotation
+ * in FP32 and row-scaled S8 quantisation (the page's "Pre-scales and SwiGLU
+ * run before rotation" and "SwiGLU is fused with rotation/A8 quantization").
+ *
+ *   x       [M][ld_x] in x_dtype (BF16 / FP16 / FP32).  swiglu == 0: columns
+ *           0..K-1 are the input.  swiglu != 0: columns 0..K-1 are the gate
+ *           g and K..2K-1 the value v, and the layer input is
+ *           h = g * sigmoid(g) * v computed in FP32 with no intermediate
+ *           rounding.  ld_x >= K (or 2K).
+ *   a_q     [M][ld_aq] codes in `fmt`, columns 0..K_p-1 written; ld_aq >= K_p.
+ *   a_scale [M] FP32 token scales s_a (0 for a degenerate row).
+ *
+ * Quantiser as for the weights (FP32 scale, FP32 reciprocal, FP32 product,
+ * round half to even, clamp to +-127).  FP16 inputs are widened to FP32
+ * before anything else.  x needs only element alignment; 16-byte aligned
+ * rows take the vectorised load path.
+ */
+int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
+                      int M, int K, int swiglu,
+                      void* a_q, convrot_codes fmt, int64_t ld_aq,
+                      float* a_scale, cudaStream_t stream);
+
+/*
+ * Integer GEMM with the dequantising epilogue (the page's "row-scaled INT8
+ * Tensor Core GEMM"; the rescale happens inside the GEMM so no int32 matrix
+ * is ever written).
+ *
+ *   a_q     [M][ld_aq] FP16-stored S8 codes of the rotated activations.
+ *   w_q     [N][ld_wq] FP16-stored S8 codes of the rotated weights.
+ *   a_scale [M], w_scale [N] FP32 row scales.
+ *   K_p     padded reduction width, a multiple of 256, <= CONVROT_MAX_KP.
+ *   out     [M][ld_out] in out_dtype; ld_out >= N.  Only columns 0..N-1 of
+ *           rows 0..M-1 are written.
+ *
+ * y[m, n] = fp32(acc) * s_a[m] * s_w[n] in FP32, rounded to out_dtype
+ * (nearest even).  acc is the exact int32 sum over K_p.
+ * Alignment: a_q and w_q 16-byte aligned with ld_aq, ld_wq multiples of 8
+ * (TMA rule); out needs only element alignment.
+ */
+int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale,
+                 const void* w_q, int64_t ld_wq, const float* w_scale,
+                 int M, int N, int K_p,
+                 void* out, convrot_dtype out_dtype, int64_t ld_out,
+                 cudaStream_t stream);
+
+/*
+ * Test hook: the same GEMM, writing the raw int32 accumulators
+ * acc[m, n] = sum_k q_a[m, k] * q_w[n, k] into acc [M][ld_acc] instead of
+ * dequantising.  Arguments and rules as convrot_gemm.
+ */
+int convrot_gemm_i32(const void* a_q, int64_t ld_aq,
+                     const void* w_q, int64_t ld_wq,
+                     int M, int N, int K_p,
+                     int32_t* acc, int64_t ld_acc, cudaStream_t stream);
+
+/*
+ * Device-side failure report.  Kernels that wait on asynchronous copies or
+ * tensor-core work give up after about two seconds, record a nonzero code in
+ * a device word and return early (their outputs are then incomplete).  This
+ * call synchronises `stream`, copies the word to *code (0 = no failure),
+ * clears it and returns CONVROT_ERR_DEVICE_TIMEOUT if it was set,
+ * CONVROT_OK otherwise.  `code` may be NULL.
+ */
+int convrot_device_error(cudaStream_t stream, int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVROT_H */

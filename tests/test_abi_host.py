@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rotated_w4a8_int8_gb300 as cr
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "convrot.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return cr.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+(convrot_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(cr.EXPORTS)
+
+
+def test_padded_k(lib):
+    assert [cr.padded_k(k) for k in (1, 255, 256, 257, 5000, 5376, 20480, 0, -3)] == \
+        [256, 256, 256, 512, 5120, 5376, 20480, 0, 0]
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert cr.status_string(s)
+    assert cr.status_string(99) == "unknown status"
+
+
+def test_quant_act_rejects_bad_arguments(lib):
+    f = lib.convrot_quant_act
+    P = 1 << 20    # fake, never dereferenced: every call below fails validation first
+    assert f(P, 0, 512, 4, 0, 0, P, 1, 512, P, 0) == 1                 # K <= 0
+    assert f(P, 0, 512, -1, 512, 0, P, 1, 512, P, 0) == 1              # M < 0
+    assert f(P, 7, 512, 4, 512, 0, P, 1, 512, P, 0) == 3               # dtype
+    assert f(P, 0, 512, 4, 512, 0, P, 5, 512, P, 0) == 3               # code format
+    assert f(P, 0, 511, 4, 512, 0, P, 1, 512, P, 0) == 1               # ld_x < K
+    assert f(P, 0, 1023, 4, 512, 1, P, 1, 512, P, 0) == 1              # ld_x < 2K (SwiGLU)
+    assert f(P, 0, 512, 4, 300, 0, P, 1, 300, P, 0) == 1               # ld_aq < K_p
+    assert f(None, 0, 512, 4, 512, 0, P, 1, 512, P, 0) == 1            # null x
+    assert f(P + 1, 0, 512, 4, 512, 0, P, 1, 512, P, 0) == 2           # misaligned bf16
+    assert f(P, 0, 70000, 4, 70000, 0, P, 1, 70144, P, 0) == 3         # K_p too large
+    assert f(P, 0, 512, 0, 512, 0, P, 1, 512, P, 0) == 0               # empty: no launch
+
+
+def test_prepare_weight_rejects_bad_arguments(lib):
+    f = lib.convrot_prepare_weight
+    P = 1 << 20
+    assert f(P, P, P, 4, 0, P, 1, 512, P, 0) == 1                      # K <= 0
+    assert f(P, P, P, 4, 512, P, 1, 256, P, 0) == 1                    # ld_wq < K_p
+    assert f(P + 4, P, P, 4, 512, P, 1, 512, P, 0) == 2                # w_fp4 not 8-aligned
+    assert f(P, P, P, 4, 512, P + 1, 1, 512, P, 0) == 2                # f16 codes misaligned
+    assert f(P, None, P, 4, 512, P, 1, 512, P, 0) == 1                 # null scales
+    assert f(P, P, P, 0, 512, P, 1, 512, P, 0) == 0                    # empty
+
+
+def test_gemm_rejects_bad_arguments(lib):
+    f = lib.convrot_gemm
+    P = 1 << 20
+    ok = dict(a=P, lda=512, sa=P, w=P, ldw=512, sw=P, M=4, N=4, Kp=512, o=P, dt=0, ldo=4)
+
+    def call(**kw):
+        d = dict(ok, **kw)
+        return f(d["a"], d["lda"], d["sa"], d["w"], d["ldw"], d["sw"], d["M"], d["N"], d["Kp"],
+                 d["o"], d["dt"], d["ldo"], 0)
+    assert call(Kp=500) == 1                 # K_p not a multiple of 256
+    assert call(Kp=0) == 1
+    assert call(lda=256) == 1                # ld < K_p
+    assert call(ldo=3) == 1                  # ld_out < N
+    assert call(dt=9) == 3
+    assert call(a=P + 8) == 2                # TMA base alignment
+    assert call(lda=520 + 4) == 2            # TMA pitch alignment
+    assert call(a=None) == 1
+    assert call(Kp=65536 + 256, lda=70000, ldw=70000) == 3
+    assert call(M=0) == 0 and call(N=0) == 0
+    g = lib.convrot_gemm_i32
+    assert g(P, 512, P, 512, 4, 4, 512, None, 4, 0) == 1
+    assert g(P, 512, P, 512, 4, 4, 512, P + 2, 4, 0) == 2
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    saved = cr._lib
+    cr._lib = None
+    try:
+        with pytest.raises(ImportError):
+            cr.load_library(str(tmp_path / "missing.so"))
+    finally:
+        cr._lib = saved

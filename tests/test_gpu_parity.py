@@ -1,0 +1,243 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bars: identical S8 operands give bit-exact int32 accumulators; S8 codes agree
+on >= 99.99% of entries with |diff| <= 1 (FP32 rotation order vs the oracle's
+FP64 rotation rounded to FP32); scales agree to 1e-6 relative; outputs are
+within relative L2 1e-3 of the oracle and within 2 BF16 ulp of the row max
+per element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import (DEV, assert_codes_match, assert_output_match, assert_scales_match,
+                      codes_to_np, ensure_built, f16_codes_from_np, gpu_gemm, gpu_prepare_weight,
+                      gpu_quant_act, storage_to_dev)
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    import rotated_w4a8_int8_gb300 as cr
+    yield
+    assert cr.device_error() == 0
+
+
+def small(name, M, N):
+    wl = synth.WORKLOADS[name]
+    return synth.Workload(f"{name}_small", M, wl.K, N, wl.x_dtype, wl.out_dtype, wl.swiglu,
+                          wl.outlier_frac, wl.outlier_mult, wl.seed)
+
+
+# ---------------------------------------------------------------- kernel 2
+ACT_CASES = [
+    ("tiny", synth.WORKLOADS["tiny"]),
+    ("qkv_rows", small("qkv", 200, 8)),
+    ("ffn_down_rows", small("ffn_down", 64, 8)),
+    ("ffn_up_rows", small("ffn_up", 96, 8)),
+    ("ragged_rows", small("ragged", 77, 8)),
+    ("wide_rows", small("wide_k", 40, 8)),
+    ("fp32_in", synth.Workload("fp32_in", 33, 1000, 8, "fp32", "fp32", False, 0.01, 20.0, 9)),
+    ("swiglu_fp16", synth.Workload("sw16", 50, 768, 8, "fp16", "bf16", True, 0.0, 1.0, 10)),
+    ("swiglu_fp32_ragged", synth.Workload("sw32", 21, 300, 8, "fp32", "bf16", True, 0.0, 1.0, 11)),
+    ("k16", synth.Workload("k16", 17, 16, 8, "bf16", "bf16", False, 0.0, 1.0, 12)),
+    ("k1", synth.Workload("k1", 5, 1, 8, "bf16", "bf16", False, 0.0, 1.0, 13)),
+]
+
+
+@pytest.mark.parametrize("case,wl", ACT_CASES, ids=[c[0] for c in ACT_CASES])
+def test_quant_act_matches_oracle(case, wl):
+    x = synth.make_activations(wl)
+    Kp = oracle.padded_k(wl.K)
+    q, s = gpu_quant_act(x, wl.x_dtype, wl.K, wl.swiglu, fmt="f16")
+    q8, s8 = gpu_quant_act(x, wl.x_dtype, wl.K, wl.swiglu, fmt="s8")
+    rq, rs = oracle.quant_act(x, wl.x_dtype, wl.K, wl.swiglu)
+    got = codes_to_np(q, Kp)
+    assert np.array_equal(got, codes_to_np(q8, Kp))
+    assert torch.equal(s, s8)
+    assert_codes_match(got, rq)
+    assert_scales_match(s.cpu().numpy(), rs)
+
+
+def test_quant_act_unaligned_pitch_and_wide_ld():
+    # bf16 pitch of K+1 elements: rows are not 16-byte aligned -> scalar path
+    wl = synth.Workload("pitch", 40, 700, 8, "bf16", "bf16", False, 0.02, 20.0, 14)
+    x = synth.make_activations(wl)
+    wide = np.zeros((wl.M, wl.K + 1), np.uint16)
+    wide[:, :wl.K] = x
+    wide[:, wl.K] = 0x7F80          # +inf in the column past K: must be ignored
+    xd = storage_to_dev(wide, "bf16")
+    Kp = oracle.padded_k(wl.K)
+    q, s = gpu_quant_act(None, "bf16", wl.K, xdev=xd, ld=Kp + 64)
+    rq, rs = oracle.quant_act(x, "bf16", wl.K)
+    assert_codes_match(codes_to_np(q, Kp), rq)
+    assert_scales_match(s.cpu().numpy(), rs)
+
+
+def test_quant_act_degenerate_rows():
+    wl = synth.Workload("deg", 6, 512, 8, "bf16", "bf16", False, 0.0, 1.0, 15)
+    x = synth.make_activations(wl)
+    x[1] = 0                        # all-zero row
+    x[3] = 0
+    x[3, 7] = 0x0001                # one bf16 subnormal: reciprocal scale overflows
+    q, s = gpu_quant_act(x, "bf16", wl.K)
+    rq, rs = oracle.quant_act(x, "bf16", wl.K)
+    got = codes_to_np(q, 512)
+    assert np.all(got[1] == 0) and np.all(got[3] == 0)
+    sc = s.cpu().numpy()
+    assert sc[1] == 0 and sc[3] == 0
+    assert_codes_match(got, rq)
+    assert_scales_match(sc, rs)
+
+
+# ---------------------------------------------------------------- kernel 1
+W_CASES = [
+    ("tiny", synth.WORKLOADS["tiny"]),
+    ("qkv_rows", small("qkv", 8, 300)),
+    ("ffn_down_rows", small("ffn_down", 8, 130)),
+    ("ragged_rows", small("ragged", 8, 257)),
+    ("wide_rows", small("wide_k", 8, 64)),
+    ("k40", synth.Workload("k40", 8, 40, 24, "bf16", "bf16", False, 0.0, 1.0, 16)),
+]
+
+
+@pytest.mark.parametrize("case,wl", W_CASES, ids=[c[0] for c in W_CASES])
+def test_prepare_weight_matches_oracle(case, wl):
+    packed, scales, t = synth.make_nvfp4_weight(wl)
+    Kp = oracle.padded_k(wl.K)
+    q, s = gpu_prepare_weight(packed, scales, t, wl.K, fmt="f16")
+    q8, s8 = gpu_prepare_weight(packed, scales, t, wl.K, fmt="s8")
+    rq, rs = oracle.prepare_weight(packed, scales, t, wl.K)
+    got = codes_to_np(q, Kp)
+    assert np.array_equal(got, codes_to_np(q8, Kp))
+    assert_codes_match(got, rq)
+    assert_scales_match(s.cpu().numpy(), rs)
+
+
+def test_prepare_weight_ignores_serialised_padding():
+    wl = small("ragged", 8, 100)          # K = 5000, K_s = 5008
+    packed, scales, t = synth.make_nvfp4_weight(wl)
+    dirty = packed.copy()
+    dirty[:, 2500:] = 0x77                # elements 5000..5007 -> code 7 (6.0)
+    qa, sa = gpu_prepare_weight(packed, scales, t, wl.K)
+    qb, sb = gpu_prepare_weight(dirty, scales, t, wl.K)
+    assert torch.equal(qa, qb) and torch.equal(sa, sb)
+
+
+# ---------------------------------------------------------------- kernel 3
+GEMM_SHAPES = [(128, 256, 256), (300, 520, 1280), (1, 1, 256), (129, 257, 768), (513, 300, 5376),
+               (64, 1000, 512)]
+
+
+@pytest.mark.parametrize("M,N,Kp", GEMM_SHAPES)
+def test_gemm_int32_bit_exact(M, N, Kp):
+    import rotated_w4a8_int8_gb300 as cr
+    rng = np.random.default_rng(M * 7 + N)
+    qa = rng.integers(-127, 128, (M, Kp)).astype(np.int8)
+    qw = rng.integers(-127, 128, (N, Kp)).astype(np.int8)
+    acc = torch.full((M, N), 12345, dtype=torch.int32, device=DEV)
+    cr.gemm_i32(f16_codes_from_np(qa), f16_codes_from_np(qw), acc)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), oracle.int_gemm(qa, qw))
+
+
+@pytest.mark.parametrize("pattern", ["all_max", "alternating", "max_minus"])
+def test_gemm_int32_exact_at_extremes(pattern):
+    # partial sums reach 127^2 * 512 inside a chunk and 127^2 * 20480 in total
+    import rotated_w4a8_int8_gb300 as cr
+    M, N, Kp = 130, 260, 20480
+    qa = np.full((M, Kp), 127, np.int8)
+    qw = np.full((N, Kp), 127, np.int8)
+    if pattern == "alternating":
+        qw[:, 1::2] = -127
+        qa[::2, :] = -127
+    elif pattern == "max_minus":
+        qw[:] = -127
+        qa[:, -1] = 126
+    acc = torch.zeros((M, N), dtype=torch.int32, device=DEV)
+    cr.gemm_i32(f16_codes_from_np(qa), f16_codes_from_np(qw), acc)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), oracle.int_gemm(qa, qw))
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp16", "fp32"])
+def test_gemm_dequant_given_identical_operands(out_dtype):
+    rng = np.random.default_rng(21)
+    M, N, Kp = 257, 384, 1024
+    qa = rng.integers(-127, 128, (M, Kp)).astype(np.int8)
+    qw = rng.integers(-127, 128, (N, Kp)).astype(np.int8)
+    sa = (rng.uniform(0.5, 2.0, M) * 1e-3).astype(np.float32)
+    sw = (rng.uniform(0.5, 2.0, N) * 1e-4).astype(np.float32)
+    sa[5] = 0
+    y = gpu_gemm(f16_codes_from_np(qa), torch.from_numpy(sa).to(DEV), f16_codes_from_np(qw),
+                 torch.from_numpy(sw).to(DEV), out_dtype, Kp)
+    ref = oracle.dequantize(oracle.int_gemm(qa, qw), sa, sw, out_dtype)
+    got = y.float().cpu().numpy().astype(np.float64)
+    assert np.all(got[5] == 0)
+    assert_output_match(got, ref)
+    # one rounding of an FP32 product chain: at most one unit in the last place
+    ulp = {"bf16": 2.0 ** -7, "fp16": 2.0 ** -10, "fp32": 2.0 ** -23}[out_dtype]
+    mag = np.maximum(np.abs(ref), 1e-30)
+    assert np.all(np.abs(got - ref) <= ulp * 2.0 ** np.floor(np.log2(mag)) * 1.0001)
+
+
+def test_gemm_output_pitch_guard_and_unaligned_base():
+    rng = np.random.default_rng(22)
+    M, N, Kp = 140, 270, 512
+    qa = rng.integers(-127, 128, (M, Kp)).astype(np.int8)
+    qw = rng.integers(-127, 128, (N, Kp)).astype(np.int8)
+    sa = np.full(M, 1e-3, np.float32)
+    sw = np.full(N, 1e-3, np.float32)
+    import rotated_w4a8_int8_gb300 as cr
+    big = torch.full((M + 1, N + 9), -7.0, dtype=torch.bfloat16, device=DEV)
+    view = big[:M, 1:N + 1]               # base 2 bytes past a 16-byte boundary
+    cr.gemm(f16_codes_from_np(qa), torch.from_numpy(sa).to(DEV), f16_codes_from_np(qw),
+            torch.from_numpy(sw).to(DEV), view, K_p=Kp)
+    b = big.float().cpu().numpy()
+    assert np.all(b[:, 0] == -7) and np.all(b[:, N + 1:] == -7) and np.all(b[M] == -7)
+    ref = oracle.dequantize(oracle.int_gemm(qa, qw), sa, sw, "bf16")
+    assert_output_match(b[:M, 1:N + 1], ref)
+
+
+def test_empty_calls_launch_nothing():
+    import rotated_w4a8_int8_gb300 as cr
+    lib = cr.load_library()
+    y = torch.full((4, 4), 3.0, device=DEV)
+    assert lib.convrot_gemm(16, 512, 16, 16, 512, 16, 0, 4, 512, y.data_ptr(), 2, 4, 0) == 0
+    assert lib.convrot_quant_act(16, 0, 512, 0, 512, 0, 16, 1, 512, 16, 0) == 0
+    torch.cuda.synchronize()
+    assert torch.all(y == 3.0)
+
+
+# ---------------------------------------------------------------- whole layer
+LAYER_CASES = [
+    ("tiny", synth.WORKLOADS["tiny"]),
+    ("qkv", small("qkv", 300, 600)),
+    ("ffn_down", small("ffn_down", 200, 300)),
+    ("ffn_up", small("ffn_up", 150, 700)),
+    ("ragged", small("ragged", 129, 517)),
+    ("wide_k", small("wide_k", 130, 260)),
+]
+
+
+def run_layer(wl, x, packed, scales, t, xdev=None):
+    Kp = oracle.padded_k(wl.K)
+    qw, sw = gpu_prepare_weight(packed, scales, t, wl.K)
+    qa, sa = gpu_quant_act(x, wl.x_dtype, wl.K, wl.swiglu, xdev=xdev)
+    y = gpu_gemm(qa, sa, qw, sw, wl.out_dtype, Kp)
+    return y, (qa, sa, qw, sw)
+
+
+@pytest.mark.parametrize("case,wl", LAYER_CASES, ids=[c[0] for c in LAYER_CASES])
+def test_layer_matches_oracle(case, wl):
+    x = synth.make_activations(wl)
+    packed, scales, t = synth.make_nvfp4_weight(wl)
+    y, (qa, sa, qw, sw) = run_layer(wl, x, packed, scales, t)
+    ref, mid = oracle.convrot_linear(x, wl.x_dtype, packed, scales, t, wl.K, wl.out_dtype, wl.swiglu)
+    Kp = oracle.padded_k(wl.K)
+    assert_codes_match(codes_to_np(qa, Kp), mid["qa"])
+    assert_codes_match(codes_to_np(qw, Kp), mid["qw"])
+    assert_output_match(y.float().cpu().numpy(), ref)
