@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the ConvRot W4A8 linear layer on GB300.
+
+One step = one whole layer at the MiniMax-H3 QKV projection shape (M = 19989
+tokens, K = 5376, N = 21504, BF16 in / BF16 out): NVFP4 weight preparation
+(decode + rotation + S8), activation rotation + S8, and the integer GEMM with
+its dequant epilogue -- the three C-ABI calls, weights re-prepared every
+call as in the layer's single runtime path.  Inputs are seeded synthetic data
+of the workload's shape and distribution, resident in HBM before timing; L2 is
+flushed (a write larger than L2) before every timed step.
+
+Prints ONE JSON line (rank 0).  `value` is effective TOPS = 2 M N K / t summed
+over ranks (replicas: every rank runs the full layer on its own GPU).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import dataclasses
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "ms/layer and effective INT8 TOPS at M=19989 (QKV, FFN-down); % of INT8/HBM roofline"
+# the pages' QKV layer time on an A40 at M=19989 (context, another machine)
+PAGES_QKV_MS = 25.08
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM traffic of one GEMM launch at the QKV shape, from the ncu capture summarised in
+# profiles/gemm_tcgen05_qkv.md, valid for the gemm.cu source with this SHA-256 prefix.
+GEMM_TRAFFIC = {"sha256_16": None, "bytes": None}
+
+
+def sha16(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- workload sizes
+def layer_sizes(wl: synth.Workload):
+    Kp = -(-wl.K // 256) * 256
+    Ks = synth.stored_k(wl.K)
+    esz = {"bf16": 2, "fp16": 2, "fp32": 4}
+    act_bytes = wl.M * wl.k_in * esz[wl.x_dtype] + wl.M * Kp * 2 + 4 * wl.M
+    w_bytes = wl.N * Ks // 2 + wl.N * Ks // 16 + 4 + wl.N * Kp * 2 + 4 * wl.N
+    return dict(Kp=Kp, Ks=Ks, ops=2.0 * wl.M * wl.N * wl.K, gemm_flops=2.0 * wl.M * wl.N * Kp,
+                act_bytes=act_bytes, w_bytes=w_bytes)
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for r in csv.reader(io.StringIO(f.read())):
+                if len(r) < 10:
+                    continue
+                r = [c.strip() for c in r]
+                if self.bus_id and self.bus_id.lower() not in r[1].lower():
+                    continue
+                rows.append(r)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- GPU layer
+class Layer:
+    """Device buffers and the three C-ABI calls of one ConvRot layer."""
+
+    def __init__(self, wl: synth.Workload, dev):
+        import torch
+
+        import rotated_w4a8_int8_gb300 as cr
+        self.cr = cr
+        self.wl = wl
+        self.sz = layer_sizes(wl)
+        t0 = time.time()
+        x = synth.make_activations(wl)
+        packed, scales, tscale = synth.make_nvfp4_weight(wl)
+        self.gen_s = time.time() - t0
+        tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+        if wl.x_dtype == "fp32":
+            xh = torch.from_numpy(x)
+        else:
+            xh = torch.from_numpy(x.view(np.int16)).view(tdt[wl.x_dtype])
+        # pinned host copies (the end-to-end leg copies them in every step)
+        self.h_x = xh.pin_memory()
+        self.h_p = torch.from_numpy(packed).pin_memory()
+        self.h_s = torch.from_numpy(scales).pin_memory()
+        self.h_t = torch.tensor([float(tscale)], dtype=torch.float32).pin_memory()
+        self.x = self.h_x.to(dev)
+        self.p = self.h_p.to(dev)
+        self.s = self.h_s.to(dev)
+        self.t = self.h_t.to(dev)
+        Kp = self.sz["Kp"]
+        self.aq = torch.empty(wl.M, Kp, dtype=torch.float16, device=dev)
+        self.sa = torch.empty(wl.M, dtype=torch.float32, device=dev)
+        self.wq = torch.empty(wl.N, Kp, dtype=torch.float16, device=dev)
+        self.sw = torch.empty(wl.N, dtype=torch.float32, device=dev)
+        self.y = torch.empty(wl.M, wl.N, dtype=tdt[wl.out_dtype], device=dev)
+        self.h_y = None
+        self.in_bytes = sum(t.numel() * t.element_size() for t in (self.h_x, self.h_p, self.h_s, self.h_t))
+
+    def weight(self):
+        self.cr.prepare_weight(self.p, self.s, self.t, self.wl.K, self.wq, self.sw)
+
+    def act(self):
+        self.cr.quant_act(self.x, self.wl.K, self.aq, self.sa, swiglu=self.wl.swiglu)
+
+    def gemm(self):
+        self.cr.gemm(self.aq, self.sa, self.wq, self.sw, self.y)
+
+    def step(self):
+        self.weight()
+        self.act()
+        self.gemm()
+
+    def e2e_step(self):
+        """Public API with host buffers: inputs in, layer, output out."""
+        import torch
+        if self.h_y is None:
+            self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
+        self.x.copy_(self.h_x, non_blocking=True)
+        self.p.copy_(self.h_p, non_blocking=True)
+        self.s.copy_(self.h_s, non_blocking=True)
+        self.t.copy_(self.h_t, non_blocking=True)
+        self.step()
+        self.h_y.copy_(self.y, non_blocking=True)
+
+
+def time_layer(layer: Layer, steps: int, warmup: int, world: int, flush, sampler=None):
+    """K timed steps; per-kernel CUDA events on the launching stream; L2 flushed
+    before every step (outside the events)."""
+    import torch
+    for _ in range(warmup):
+        flush()
+        layer.step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        ev[i][0].record()
+        layer.weight()
+        ev[i][1].record()
+        layer.act()
+        ev[i][2].record()
+        layer.gemm()
+        ev[i][3].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    w = [e[0].elapsed_time(e[1]) for e in ev]
+    a = [e[1].elapsed_time(e[2]) for e in ev]
+    g = [e[2].elapsed_time(e[3]) for e in ev]
+    tot = [e[0].elapsed_time(e[3]) for e in ev]
+    return dict(total_ms=sum(tot), step_ms=tot, weight_ms=w, act_ms=a, gemm_ms=g, clocks=clocks)
+
+
+def time_e2e(layer: Layer, steps: int, warmup: int, world: int):
+    import torch
+    for _ in range(warmup):
+        layer.e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        layer.e2e_step()
+    e.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return s.elapsed_time(e)
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+class OracleSample:
+    """The first m tokens x first n weight rows of a workload, generated once;
+    timing covers only the oracle's whole layer on them."""
+
+    def __init__(self, wl: synth.Workload, m_max: int, n_max: int):
+        self.wl = wl
+        self.m_max, self.n_max = min(wl.M, m_max), min(wl.N, n_max)
+        self.x = synth.make_activations(wl, rows=self.m_max)
+        self.packed, self.scales, self.t = synth.make_nvfp4_weight(wl, rows=self.n_max)
+
+    def time(self, m: int, n: int) -> float:
+        import oracle
+        wl = self.wl
+        m, n = min(m, self.m_max), min(n, self.n_max)
+        t0 = time.perf_counter()
+        oracle.convrot_linear(self.x[:m], wl.x_dtype, self.packed[:n], self.scales[:n], self.t,
+                              wl.K, wl.out_dtype, wl.swiglu)
+        return time.perf_counter() - t0
+
+
+def calibrate(sample: OracleSample, target_s: float):
+    """Grows (m, n) from a small probe until one oracle pass takes about target_s."""
+    m, n = 64, 256
+    t = sample.time(m, n)
+    while t < 0.5 * target_s and (m < sample.m_max or n < sample.n_max):
+        f = min(4.0, max(1.25, (target_s / max(t, 1e-3)) ** 0.5))
+        m, n = int(min(sample.m_max, m * f)), int(min(sample.n_max, n * f))
+        t = sample.time(m, n)
+    return m, n, t
+
+
+def cpu_baseline(wl: synth.Workload, budget_s: float):
+    sample = OracleSample(wl, 4096, 16384)
+    m, n, t = calibrate(sample, budget_s)
+    ops = 2.0 * m * n * wl.K
+    cores = len(os.sched_getaffinity(0))
+    return {"value": ops / t / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{wl.name}: first {m} of {wl.M} tokens x first {n} of {wl.N} weight rows, "
+                      f"full K={wl.K}, whole layer (decode, rotation, S8, int GEMM, dequant) in "
+                      f"numpy FP64; {t:.2f} s; BLAS threads = cores, elementwise single-threaded",
+            "seconds": t}
+
+
+def reference_arm(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = min(10.0, max(0.2, 150.0 / max(1, args.steps + args.warmup)))
+    sample = OracleSample(wl, 2048, 8192)
+    m_s, n_s, _ = calibrate(sample, per_step)
+    for _ in range(args.warmup):
+        sample.time(m_s, n_s)
+    ts = [sample.time(m_s, n_s) for _ in range(args.steps)]
+    ops = 2.0 * m_s * n_s * wl.K
+    value = ops * len(ts) / sum(ts) / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample_txt = (f"{wl.name}: first {m_s} of {wl.M} tokens x first {n_s} of {wl.N} weight rows "
+                  f"per step, full K={wl.K}, numpy FP64 oracle, whole layer")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(ts) / len(ts), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{wl.name} M={wl.M} K={wl.K} N={wl.N}", "sample": sample_txt},
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample_txt},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qkv", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--secondary", default="ffn_down",
+                    help="second workload timed in the same run ('' to skip)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="truncate M to this many tokens (small profiling case; not a bench line)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    wl = synth.WORKLOADS[args.workload]
+    if args.rows > 0:
+        wl = dataclasses.replace(wl, name=f"{wl.name}_rows{args.rows}", M=min(wl.M, args.rows))
+    if args.impl == "reference":
+        reference_arm(args, wl)
+        return
+
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    bus = getattr(props, "pci_bus_id", None)
+    if isinstance(bus, int):
+        bus = None
+    peaks, peaks_src = load_peaks()
+
+    layer = Layer(wl, dev)
+    sz = layer.sz
+    r = time_layer(layer, args.steps, args.warmup, world, flush, ClockSampler(bus))
+    t_max = reduce_max(r["total_ms"], world)
+    ms_step = t_max / args.steps
+    value = world * sz["ops"] * args.steps / (t_max / 1e3) / 1e12
+    g_ms = statistics.mean(r["gemm_ms"])
+    a_ms = statistics.mean(r["act_ms"])
+    w_ms = statistics.mean(r["weight_ms"])
+    achieved = sz["gemm_flops"] / (g_ms / 1e3) / 1e12
+    peak_t = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gemm_src = os.path.join(ROOT, "rotated_w4a8_int8_gb300", "csrc", "gemm.cu")
+    traffic = GEMM_TRAFFIC["bytes"] if GEMM_TRAFFIC["sha256_16"] == sha16(gemm_src) else None
+
+    # end-to-end through the public API with host buffers
+    e2e_value = e2e_ms = None
+    if args.e2e_steps > 0:
+        e2e_ms = reduce_max(time_e2e(layer, args.e2e_steps, 3, world), world)
+        e2e_value = world * sz["ops"] * args.e2e_steps / (e2e_ms / 1e3) / 1e12
+    d2h = layer.y.numel() * layer.y.element_size()
+    if layer.cr.device_error() != 0:
+        raise SystemExit("device timeout reported by the GEMM")
+
+    kernels = {
+        "prepare_weight": {"us": 1e3 * w_ms, "bytes": sz["w_bytes"],
+                           "gbs": sz["w_bytes"] / (w_ms / 1e3) / 1e9},
+        "quant_act": {"us": 1e3 * a_ms, "bytes": sz["act_bytes"],
+                      "gbs": sz["act_bytes"] / (a_ms / 1e3) / 1e9},
+        "gemm": {"ms": g_ms, "tflops": achieved},
+    }
+    for k in ("prepare_weight", "quant_act"):
+        kernels[k]["hbm_frac"] = kernels[k]["gbs"] / hbm
+    del layer
+    torch.cuda.empty_cache()
+
+    secondary = None
+    if args.secondary:
+        wl2 = synth.WORKLOADS[args.secondary]
+        l2y = Layer(wl2, dev)
+        r2 = time_layer(l2y, max(10, args.steps // 4), args.warmup, world, flush)
+        s2 = l2y.sz
+        ms2 = reduce_max(r2["total_ms"], world) / len(r2["step_ms"])
+        g2 = statistics.mean(r2["gemm_ms"])
+        a2 = statistics.mean(r2["act_ms"])
+        w2 = statistics.mean(r2["weight_ms"])
+        secondary = {"workload": f"{wl2.name} M={wl2.M} K={wl2.K} (SwiGLU input {wl2.k_in}) N={wl2.N}"
+                     if wl2.swiglu else f"{wl2.name} M={wl2.M} K={wl2.K} N={wl2.N}",
+                     "ms_per_layer": ms2, "eff_tops": s2["ops"] / (ms2 / 1e3) / 1e12,
+                     "gemm_ms": g2, "gemm_tflops": s2["gemm_flops"] / (g2 / 1e3) / 1e12,
+                     "quant_act_us": 1e3 * a2, "quant_act_gbs": s2["act_bytes"] / (a2 / 1e3) / 1e9,
+                     "prepare_weight_us": 1e3 * w2,
+                     "prepare_weight_gbs": s2["w_bytes"] / (w2 / 1e3) / 1e9,
+                     "pages_a40_ms": 19.49}
+        del l2y
+        torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        cpu = cpu_baseline(wl, args.cpu_budget)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": value / world / (sz["ops"] / (PAGES_QKV_MS / 1e3) / 1e12),
+        "dtype": "s8", "data": "synthetic",
+        "config": {"workload": f"{wl.name} M={wl.M} K={wl.K} N={wl.N} {wl.x_dtype}->{wl.out_dtype}",
+                   "layer": "NVFP4 weight prep + act rotation/S8 + GEMM per step",
+                   "l2": f"flushed before every step ({flush_buf.numel() * 4 >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}",
+                   "arith": "S8 codes held as FP16 on tcgen05 kind::f16, exact int32 via 512-K FP32 chunks; "
+                            "FP32 rotation"},
+        "ms_per_layer": ms_step,
+        "kernels": kernels,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": achieved / peak_t, "traffic": traffic,
+                     "kernel": "gemm (tcgen05 kind::f16)",
+                     "peak_source": f"{peaks_src} bf16_tflops_sustained (FP16 = BF16 rate)",
+                     "work_per_launch": f"2*M*N*K_p = {sz['gemm_flops']:.4e} FLOP"},
+        "hbm_peak_gbs": hbm,
+        "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": layer_in_bytes(wl),
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None},
+        "gpu_launches": 3 * args.steps,
+        "clocks": r["clocks"],
+        "cpu_baseline": cpu,
+        "secondary": secondary,
+        "vs_baseline_note": "value / the pages' A40 QKV layer (25.08 ms = 184.3 TOPS): context only",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def layer_in_bytes(wl):
+    esz = {"bf16": 2, "fp16": 2, "fp32": 4}[wl.x_dtype]
+    Ks = synth.stored_k(wl.K)
+    return wl.M * wl.k_in * esz + wl.N * Ks // 2 + wl.N * Ks // 16 + 4
+
+
+if __name__ == "__main__":
+    main()

@@ -21,145 +21,197 @@ namespace convrot {
 // ------------------------------------------------------------------ loaders
 enum : int { DT_BF16 = 0, DT_FP16 = 1, DT_FP32 = 2 };
 
+// Raw storage words of the 32 elements [c0, c0 + 32) a thread owns in pass 1
+// (rows 2p and 2p+1 of its block).  16-bit types: word k holds elements 2k,
+// 2k+1; FP32: word k holds element k.
 template <int DT>
-__device__ __forceinline__ float load_scalar(const void* row, int k) {
-  if constexpr (DT == DT_BF16) {
-    const uint16_t b = static_cast<const uint16_t*>(row)[k];
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
-  } else if constexpr (DT == DT_FP16) {
-    return __half2float(static_cast<const __half*>(row)[k]);
-  } else {
-    return static_cast<const float*>(row)[k];
-  }
+struct Raw {
+  static constexpr int N = (DT == DT_FP32) ? 32 : 16;
+  uint32_t w[N];
+};
+
+template <int DT>
+__device__ __forceinline__ uint32_t load_elem_bits(const char* row, int k) {
+  if constexpr (DT == DT_FP32) return reinterpret_cast<const uint32_t*>(row)[k];
+  else return reinterpret_cast<const uint16_t*>(row)[k];
 }
 
-__device__ __forceinline__ void unpack_bf16x2(uint32_t w, float& lo, float& hi) {
-  lo = __uint_as_float(w << 16);
-  hi = __uint_as_float(w & 0xffff0000u);
-}
-
-__device__ __forceinline__ void unpack_f16x2(uint32_t w, float& lo, float& hi) {
-  __half2 h = *reinterpret_cast<__half2*>(&w);
-  float2 f = __half22float2(h);
-  lo = f.x;
-  hi = f.y;
-}
-
-// 16 consecutive elements x[c0 .. c0+15] of one row, zero beyond K.
 template <int DT, bool VEC>
-__device__ __forceinline__ void load16(const void* row, int c0, int K, float (&v)[16]) {
+__device__ __forceinline__ void load_raw(const char* row, int c0, int K, Raw<DT>& r) {
   if (c0 >= K) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+    for (int i = 0; i < Raw<DT>::N; ++i) r.w[i] = 0u;
     return;
   }
-  if (VEC && c0 + 16 <= K) {
-    if constexpr (DT == DT_FP32) {
-      const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(row) + c0);
+  if (VEC && c0 + 32 <= K) {
+    constexpr int esz = (DT == DT_FP32) ? 4 : 2;
+    const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<size_t>(c0) * esz);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float4 f = __ldg(p + u);
-        v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
-      }
-    } else {
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(row) + c0);
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        uint4 w = __ldg(p + u);
-        uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if constexpr (DT == DT_BF16) unpack_bf16x2(ws[j], v[8 * u + 2 * j], v[8 * u + 2 * j + 1]);
-          else unpack_f16x2(ws[j], v[8 * u + 2 * j], v[8 * u + 2 * j + 1]);
-        }
-      }
+    for (int u = 0; u < Raw<DT>::N / 4; ++u) {
+      const uint4 v = __ldg(p + u);
+      r.w[4 * u] = v.x; r.w[4 * u + 1] = v.y; r.w[4 * u + 2] = v.z; r.w[4 * u + 3] = v.w;
     }
     return;
   }
+  if constexpr (DT == DT_FP32) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = (c0 + i < K) ? load_scalar<DT>(row, c0 + i) : 0.f;
+    for (int e = 0; e < 32; ++e) r.w[e] = (c0 + e < K) ? load_elem_bits<DT>(row, c0 + e) : 0u;
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t lo = (c0 + 2 * k < K) ? load_elem_bits<DT>(row, c0 + 2 * k) : 0u;
+      const uint32_t hi = (c0 + 2 * k + 1 < K) ? load_elem_bits<DT>(row, c0 + 2 * k + 1) : 0u;
+      r.w[k] = lo | (hi << 16);
+    }
+  }
 }
 
-// E4M3 ("FN") byte -> float, through the hardware FP8 -> FP16 conversion (exact).
-__device__ __forceinline__ float e4m3_to_float(uint8_t b) {
+// Element e (0..31) of a Raw as FP32.
+template <int DT>
+__device__ __forceinline__ float raw_elem(const Raw<DT>& r, int e) {
+  if constexpr (DT == DT_FP32) {
+    return __uint_as_float(r.w[e]);
+  } else if constexpr (DT == DT_BF16) {
+    const uint32_t w = r.w[e >> 1];
+    return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+  } else {
+    const uint32_t w = r.w[e >> 1];
+    return __half2float(__ushort_as_half(static_cast<unsigned short>((e & 1) ? (w >> 16) : (w & 0xffffu))));
+  }
+}
+
+// Pass-1 pairs P[b] = (x[2p][b], x[2p+1][b]) = (elem b, elem 16 + b).
+template <int DT>
+__device__ __forceinline__ void pairs_from_raw(const Raw<DT>& r, float2 (&P)[16]) {
+#pragma unroll
+  for (int b = 0; b < 16; ++b) P[b] = make_float2(raw_elem<DT>(r, b), raw_elem<DT>(r, 16 + b));
+}
+
+// SwiGLU h = g * sigmoid(g) * v in FP32 (no intermediate rounding to the input dtype).
+__device__ __forceinline__ float swiglu1(float g, float v) {
+  return __fdividef(g, 1.0f + expf(-g)) * v;
+}
+
+template <int DT>
+__device__ __forceinline__ void pairs_swiglu(const Raw<DT>& g, const Raw<DT>& v, float2 (&P)[16]) {
+#pragma unroll
+  for (int b = 0; b < 16; ++b)
+    P[b] = make_float2(swiglu1(raw_elem<DT>(g, b), raw_elem<DT>(v, b)),
+                       swiglu1(raw_elem<DT>(g, 16 + b), raw_elem<DT>(v, 16 + b)));
+}
+
+// NVFP4: two E2M1 codes (one byte, element 2j in the low nibble) -> FP16x2,
+// through the hardware FP4 conversion (exact).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Two E4M3 ("FN") scale bytes -> two floats (exact).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
   uint32_t h2;
-  const uint16_t pair = b;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
-  __half2 h = *reinterpret_cast<__half2*>(&h2);
-  return __low2float(h);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
 }
 
-// 16 decoded NVFP4 elements of chunk c0/16, WITHOUT the tensor scale:
-// u = E2M1 * E4M3, exact in FP32.  Elements >= K (serialised padding or
-// beyond the stored row) are zero.
-__device__ __forceinline__ void load16_nvfp4(const uint8_t* prow, const uint8_t* srow, int c0,
-                                             int K, float (&u)[16]) {
+// Pass-1 pairs of a weight block chunk: the 32 decoded NVFP4 elements
+// [c0, c0 + 32) WITHOUT the tensor scale, u = E2M1 * E4M3 (exact in FP32);
+// elements >= K are zero (serialised padding is ignored).
+__device__ __forceinline__ void load_pairs_nvfp4(const uint8_t* prow, const uint8_t* srow, int c0,
+                                                 int K, int K_s, float2 (&P)[16]) {
   if (c0 >= K) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) u[i] = 0.f;
+    for (int b = 0; b < 16; ++b) P[b] = make_float2(0.f, 0.f);
     return;
   }
-  const uint2 pk = __ldg(reinterpret_cast<const uint2*>(prow + (c0 >> 1)));
-  const float half_scale = e4m3_to_float(__ldg(srow + (c0 >> 4))) * 0.5f;
+  const bool second = c0 + 16 < K_s;          // elements c0+16.. are stored
+  const uint2 w0 = __ldg(reinterpret_cast<const uint2*>(prow + (c0 >> 1)));
+  const uint2 w1 = second ? __ldg(reinterpret_cast<const uint2*>(prow + (c0 >> 1) + 8)) : make_uint2(0u, 0u);
+  // scale rows are K_s/16 bytes long (odd for some K): read the two bytes separately
+  const uint16_t sc = static_cast<uint16_t>(
+      __ldg(srow + (c0 >> 4)) | (second ? static_cast<uint32_t>(__ldg(srow + (c0 >> 4) + 1)) << 8 : 0u));
+  // scales of row 2p (elements c0..c0+15) and row 2p+1 (c0+16..c0+31)
+  const float2 scl = e4m3x2_to_float2(sc);
+  uint32_t h0[8], h1[8];
+  e2m1x8_to_f16x2(w0.x, *reinterpret_cast<uint32_t(*)[4]>(&h0[0]));
+  e2m1x8_to_f16x2(w0.y, *reinterpret_cast<uint32_t(*)[4]>(&h0[4]));
+  e2m1x8_to_f16x2(w1.x, *reinterpret_cast<uint32_t(*)[4]>(&h1[0]));
+  e2m1x8_to_f16x2(w1.y, *reinterpret_cast<uint32_t(*)[4]>(&h1[4]));
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t word = (i < 8) ? pk.x : pk.y;
-    const uint32_t nib = (word >> (4 * (i & 7))) & 0xFu;
-    // twice the E2M1 magnitude of codes 0..7 is 0,1,2,3,4,6,8,12 (one nibble each)
-    const uint32_t mag2 = (0xC8643210u >> ((nib & 7u) * 4u)) & 0xFu;
-    float val = static_cast<float>(mag2) * half_scale;
-    if (nib & 8u) val = -val;
-    u[i] = (c0 + i < K) ? val : 0.f;
+  for (int k = 0; k < 8; ++k) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h0[k]));   // row 2p: 2k, 2k+1
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&h1[k]));   // row 2p+1
+    P[2 * k] = mul2(make_float2(a.x, b.x), scl);
+    P[2 * k + 1] = mul2(make_float2(a.y, b.y), scl);
+  }
+  if (c0 + 32 > K) {                          // partial chunk: drop elements >= K
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      if (c0 + b >= K) P[b].x = 0.f;
+      if (c0 + 16 + b >= K) P[b].y = 0.f;
+    }
   }
 }
 
 // ------------------------------------------------------------------ kernels
-// Kernel 2: one CTA per token row.  Thread t: slot = t / 16 rotates blocks
-// slot, slot + S, slot + 2S, ... (at most NBMAX of them).
+// Kernel 2: one CTA per token row.  Slot s (threads 8s .. 8s+7) rotates
+// blocks s, s + S, s + 2S, ... (at most NBMAX).
 template <int DT, bool SWIGLU, int NBMAX, bool VEC>
 __global__ void __launch_bounds__(kMaxThreads)
 quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int K, int nblocks, int S,
                  void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
-  __shared__ __align__(16) float smem[(kMaxThreads / 16) * kSlotFloats];
-  __shared__ float red[kMaxThreads / 32];
+  extern __shared__ __align__(16) char smem[];
+  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);
   const int row = blockIdx.x;
-  const int slot = threadIdx.x >> 4, lane16 = threadIdx.x & 15;
-  const size_t esize = (DT == DT_FP32) ? 4 : 2;
+  const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
+  constexpr size_t esize = (DT == DT_FP32) ? 4 : 2;
   const char* xrow = static_cast<const char*>(x) + static_cast<size_t>(row) * ld_x * esize;
-  float* my = smem + slot * kSlotFloats;
+  char* my = smem + slot * kSlotBytes;
 
-  float v[NBMAX][16];
+  Raw<DT> raw[NBMAX];
+  Raw<DT> rawv[SWIGLU ? NBMAX : 1];
+#pragma unroll
+  for (int i = 0; i < NBMAX; ++i) {          // issue every load of the row first
+    const int blk = slot + S * i;
+    if (slot < S && blk < nblocks) {
+      const int c0 = blk * kBlock + 32 * lane8;
+      load_raw<DT, VEC>(xrow, c0, K, raw[i]);
+      if constexpr (SWIGLU) load_raw<DT, VEC>(xrow + static_cast<size_t>(K) * esize, c0, K, rawv[i]);
+    }
+  }
+  BlockCols c[NBMAX];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int blk = slot + S * i;
     const bool active = (slot < S) && (blk < nblocks);
+    float2 P[16];
     if (active) {
-      const int c0 = blk * kBlock + 16 * lane16;
-      if constexpr (SWIGLU) {
-        float g[16], val[16];
-        load16<DT, VEC>(xrow, c0, K, g);
-        load16<DT, VEC>(xrow + static_cast<size_t>(K) * esize, c0, K, val);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[i][e] = __fmul_rn(__fdiv_rn(g[e], 1.0f + expf(-g[e])), val[e]);
-      } else {
-        load16<DT, VEC>(xrow, c0, K, v[i]);
-      }
+      if constexpr (SWIGLU) pairs_swiglu<DT>(raw[i], rawv[SWIGLU ? i : 0], P);
+      else pairs_from_raw<DT>(raw[i], P);
     }
-    rotate_block(v[i], my, lane16, active);
-    if (active) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
-    }
+    rotate_block(P, c[i], my, lane8, active);
+    if (active) amax = absmax_cols(amax, c[i]);
   }
-  const RowQuant rq(cta_absmax(amax, red));
+  // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
+  const RowQuant rq(cta_absmax(amax, red) * 0.0625f);
   if (threadIdx.x == 0) scale[row] = rq.s;
   const size_t qsize = f16_codes ? 2 : 1;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * qsize;
+  const float mult = rq.r * 0.0625f;         // fp32(z * (r / 16)) == fp32((z / 16) * r)
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int blk = slot + S * i;
-    if (slot < S && blk < nblocks) store_codes(qrow, f16_codes, blk, lane16, v[i], rq);
+    if (slot < S && blk < nblocks) {
+      scale_cols(c[i], mult);
+      store_codes(qrow, f16_codes, blk, lane8, c[i]);
+    }
   }
 }
 
@@ -169,29 +221,28 @@ __global__ void __launch_bounds__(kMaxThreads)
 prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restrict__ w_sf,
                       const float* __restrict__ tscale, int K, int K_s, int nblocks, int S,
                       void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
-  __shared__ __align__(16) float smem[(kMaxThreads / 16) * kSlotFloats];
-  __shared__ float red[kMaxThreads / 32];
+  extern __shared__ __align__(16) char smem[];
+  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);
   const int row = blockIdx.x;
-  const int slot = threadIdx.x >> 4, lane16 = threadIdx.x & 15;
+  const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
   const uint8_t* prow = w_fp4 + static_cast<size_t>(row) * (K_s >> 1);
   const uint8_t* srow = w_sf + static_cast<size_t>(row) * (K_s >> 4);
-  const float t = __ldg(tscale);
-  float* my = smem + slot * kSlotFloats;
+  // rotated weight = fp32(z * t / 16); t / 16 is exact
+  const float t16 = __ldg(tscale) * 0.0625f;
+  char* my = smem + slot * kSlotBytes;
 
-  float v[NBMAX][16];
+  BlockCols c[NBMAX];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int blk = slot + S * i;
     const bool active = (slot < S) && (blk < nblocks);
-    if (active) load16_nvfp4(prow, srow, blk * kBlock + 16 * lane16, K, v[i]);
-    rotate_block(v[i], my, lane16, active);
+    float2 P[16];
+    if (active) load_pairs_nvfp4(prow, srow, blk * kBlock + 32 * lane8, K, K_s, P);
+    rotate_block(P, c[i], my, lane8, active);
     if (active) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        v[i][e] = __fmul_rn(v[i][e], t);           // rotated weight in FP32
-        amax = fmaxf(amax, fabsf(v[i][e]));
-      }
+      scale_cols(c[i], t16);
+      amax = absmax_cols(amax, c[i]);
     }
   }
   const RowQuant rq(cta_absmax(amax, red));
@@ -201,38 +252,56 @@ prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int blk = slot + S * i;
-    if (slot < S && blk < nblocks) store_codes(qrow, f16_codes, blk, lane16, v[i], rq);
+    if (slot < S && blk < nblocks) {
+      scale_cols(c[i], rq.r);
+      store_codes(qrow, f16_codes, blk, lane8, c[i]);
+    }
   }
 }
 
 // ------------------------------------------------------------------ launch geometry
 struct RowGeometry {
   int nblocks, nbmax, S, threads;
+  size_t smem;
 };
 
-// At most 32 slots (512 threads) per row; each slot rotates ceil(nblocks/32)
-// blocks, held in registers (NBMAX = 1, 2, 4 or 8 -> K_p <= 65536).
+// At most 64 slots (512 threads) per row; each slot rotates ceil(nblocks/64)
+// blocks, held in registers (NBMAX = 1, 2 or 4 -> K_p <= 65536).
 static bool row_geometry(int K_p, RowGeometry* g) {
   g->nblocks = K_p / kBlock;
-  const int nb = (g->nblocks + 31) / 32;
-  if (nb > 8) return false;
-  g->nbmax = nb <= 1 ? 1 : nb <= 2 ? 2 : nb <= 4 ? 4 : 8;
+  const int nb = (g->nblocks + kMaxSlots - 1) / kMaxSlots;
+  if (nb > 4) return false;
+  g->nbmax = nb <= 1 ? 1 : nb <= 2 ? 2 : 4;
   g->S = (g->nblocks + nb - 1) / nb;
-  g->threads = ((16 * g->S + 31) / 32) * 32;
+  g->threads = ((kSlotThreads * g->S + 31) / 32) * 32;
+  g->smem = static_cast<size_t>(g->S) * kSlotBytes + (kMaxThreads / 32) * sizeof(float);
   return true;
+}
+
+template <typename Kern>
+static cudaError_t prep_smem(Kern k, size_t smem) {
+  if (smem <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+}
+
+template <int DT, bool SWIGLU, bool VEC, int NB>
+static cudaError_t launch_act_nb(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
+                                 void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
+  auto k = quant_act_kernel<DT, SWIGLU, NB, VEC>;
+  cudaError_t e = prep_smem(k, g.smem);
+  if (e != cudaSuccess) return e;
+  k<<<M, g.threads, g.smem, st>>>(x, ld_x, K, g.nblocks, g.S, q, f16, ld_q, scale);
+  return cudaGetLastError();
 }
 
 template <int DT, bool SWIGLU, bool VEC>
 static cudaError_t launch_act_dt(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
                                  void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
-  dim3 grid(M), block(g.threads);
   switch (g.nbmax) {
-    case 1: quant_act_kernel<DT, SWIGLU, 1, VEC><<<grid, block, 0, st>>>(x, ld_x, K, g.nblocks, g.S, q, f16, ld_q, scale); break;
-    case 2: quant_act_kernel<DT, SWIGLU, 2, VEC><<<grid, block, 0, st>>>(x, ld_x, K, g.nblocks, g.S, q, f16, ld_q, scale); break;
-    case 4: quant_act_kernel<DT, SWIGLU, 4, VEC><<<grid, block, 0, st>>>(x, ld_x, K, g.nblocks, g.S, q, f16, ld_q, scale); break;
-    default: quant_act_kernel<DT, SWIGLU, 8, VEC><<<grid, block, 0, st>>>(x, ld_x, K, g.nblocks, g.S, q, f16, ld_q, scale); break;
+    case 1: return launch_act_nb<DT, SWIGLU, VEC, 1>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    case 2: return launch_act_nb<DT, SWIGLU, VEC, 2>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    default: return launch_act_nb<DT, SWIGLU, VEC, 4>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
   }
-  return cudaGetLastError();
 }
 
 template <int DT>
@@ -245,6 +314,17 @@ static cudaError_t launch_act(const RowGeometry& g, int M, const void* x, int64_
   }
   return vec ? launch_act_dt<DT, false, true>(g, M, x, ld_x, K, q, f16, ld_q, scale, st)
              : launch_act_dt<DT, false, false>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+}
+
+template <int NB>
+static cudaError_t launch_weight_nb(const RowGeometry& g, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
+                                    const float* t, int K, int K_s, void* q, int f16, int64_t ld_q,
+                                    float* scale, cudaStream_t st) {
+  auto k = prepare_weight_kernel<NB>;
+  cudaError_t e = prep_smem(k, g.smem);
+  if (e != cudaSuccess) return e;
+  k<<<N, g.threads, g.smem, st>>>(w_fp4, w_sf, t, K, K_s, g.nblocks, g.S, q, f16, ld_q, scale);
+  return cudaGetLastError();
 }
 
 }  // namespace convrot
@@ -266,7 +346,8 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
   if (!x || !a_q || !a_scale) return CONVROT_ERR_INVALID_ARG;
   const size_t esize = x_dtype == CONVROT_FP32 ? 4 : 2;
   if (reinterpret_cast<uintptr_t>(x) % esize) return CONVROT_ERR_MISALIGNED;
-  if (fmt == CONVROT_CODES_F16 && reinterpret_cast<uintptr_t>(a_q) % 2) return CONVROT_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(a_q) % (fmt == CONVROT_CODES_F16 ? 4 : 2) || ld_aq % 2)
+    return CONVROT_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(a_scale) % 4) return CONVROT_ERR_MISALIGNED;
   // vector path: every row start and the value half (SwiGLU) 16-byte aligned
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
@@ -298,17 +379,17 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
   if (reinterpret_cast<uintptr_t>(w_fp4) % 8 || reinterpret_cast<uintptr_t>(w_tensor_scale) % 4 ||
       reinterpret_cast<uintptr_t>(w_scale) % 4)
     return CONVROT_ERR_MISALIGNED;
-  if (fmt == CONVROT_CODES_F16 && reinterpret_cast<uintptr_t>(w_q) % 2) return CONVROT_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(w_q) % (fmt == CONVROT_CODES_F16 ? 4 : 2) || ld_wq % 2)
+    return CONVROT_ERR_MISALIGNED;
   RowGeometry g;
   if (!row_geometry(K_p, &g)) return CONVROT_ERR_UNSUPPORTED;
   const int K_s = ((K + 15) / 16) * 16;
   const int f16 = fmt == CONVROT_CODES_F16;
-  dim3 grid(N), block(g.threads);
+  cudaError_t e;
   switch (g.nbmax) {
-    case 1: prepare_weight_kernel<1><<<grid, block, 0, stream>>>(w_fp4, w_sf, w_tensor_scale, K, K_s, g.nblocks, g.S, w_q, f16, ld_wq, w_scale); break;
-    case 2: prepare_weight_kernel<2><<<grid, block, 0, stream>>>(w_fp4, w_sf, w_tensor_scale, K, K_s, g.nblocks, g.S, w_q, f16, ld_wq, w_scale); break;
-    case 4: prepare_weight_kernel<4><<<grid, block, 0, stream>>>(w_fp4, w_sf, w_tensor_scale, K, K_s, g.nblocks, g.S, w_q, f16, ld_wq, w_scale); break;
-    default: prepare_weight_kernel<8><<<grid, block, 0, stream>>>(w_fp4, w_sf, w_tensor_scale, K, K_s, g.nblocks, g.S, w_q, f16, ld_wq, w_scale); break;
+    case 1: e = launch_weight_nb<1>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
+    case 2: e = launch_weight_nb<2>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
+    default: e = launch_weight_nb<4>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
   }
-  return cudaGetLastError() == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
+  return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
 }

@@ -1,15 +1,28 @@
 // Shared device code of the two ConvRot256 rotation + row-scaled S8 kernels.
 //
-// One CTA owns one row.  The padded row is split into 256-element blocks; a
-// half-warp ("slot") of 16 threads rotates one block at a time.  The
-// Sylvester Walsh-Hadamard matrix factorises as H_256 = H_16 (x) H_16 over
-// the index j = 16 a + b, so the rotation runs in two register passes:
-//   pass 1: thread a holds x[16a + 0..15] and transforms over b;
-//   a swizzled shared-memory transpose inside the half-warp;
-//   pass 2: thread b holds column b (x[16*0..15 + b]) and transforms over a.
-// The result is scaled by 1/16, exactly.  After all blocks of the row are
-// rotated (values stay in registers), the CTA reduces the row absmax, derives
-// the FP32 scale and its FP32 reciprocal, and writes the S8 codes.
+// One CTA owns one row.  The padded row is split into 256-element blocks;
+// a group of 8 threads ("slot") rotates one block at a time.  The Sylvester
+// Walsh-Hadamard matrix factorises as H_256 = H_16 (x) H_16 over the index
+// j = 16 a + b (a: block "row", b: block "column"), so the rotation is two
+// 16-point passes with one transpose through shared memory:
+//
+//   pass 1: thread p holds rows 2p and 2p+1 as 16 FP32 pairs
+//           P[b] = (x[2p][b], x[2p+1][b]) and transforms over b -- every
+//           butterfly is one packed FP32x2 add or sub;
+//   transpose: P[b] goes to shared memory as 8-byte units, rows padded to 18
+//           units so that both sides use base + immediate addresses and the
+//           16-byte reads are free of bank conflicts;
+//   pass 2: thread q reads columns 2q and 2q+1 as pairs U[p] = (x[2p][2q],
+//           x[2p+1][2q]) and V[p] = (x[2p][2q+1], x[2p+1][2q+1]) and
+//           transforms over a = 2p + s: one scalar stage over s, three packed
+//           stages over p.
+//
+// The result is the unnormalised transform z = x H; the rotation x R with
+// R = H/16 is z * (1/16), an exact power-of-two scaling that is folded into
+// the multiplier applied afterwards.  After all blocks of the row are
+// transformed (they stay in registers), the CTA reduces the row absmax and
+// writes the S8 codes; thread q of a slot owns the code pairs at columns
+// (2q, 2q+1) of every block row.
 #pragma once
 
 #include <cstdint>
@@ -19,55 +32,117 @@
 namespace convrot {
 
 constexpr int kBlock = 256;
-constexpr int kSlotFloats = kBlock + 16;   // +16 floats: adjacent slots use opposite bank halves
+constexpr int kSlotThreads = 8;                 // threads rotating one block
 constexpr int kMaxThreads = 512;
+constexpr int kMaxSlots = kMaxThreads / kSlotThreads;
+constexpr int kRowUnits = 18;                   // 16 units of 8 bytes + 2 pad
+constexpr int kSlotBytes = 8 * kRowUnits * 8;   // 1152 bytes per slot
 
-// Unnormalised 16-point Walsh-Hadamard transform (Sylvester order), in place.
-__device__ __forceinline__ void fwht16(float (&v)[16]) {
+// ------------------------------------------------------------------ packed FP32x2
+__device__ __forceinline__ unsigned long long u64_of(float2 v) {
+  return *reinterpret_cast<unsigned long long*>(&v);
+}
+__device__ __forceinline__ float2 f2_of(unsigned long long v) {
+  return *reinterpret_cast<float2*>(&v);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+  return f2_of(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+  return f2_of(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
+  return f2_of(d);
+}
+
+// 16-point unnormalised Walsh-Hadamard transform over the array index,
+// applied to both lanes of every pair at once.
+__device__ __forceinline__ void fwht16x2(float2 (&P)[16]) {
 #pragma unroll
   for (int h = 1; h < 16; h <<= 1) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       if ((i & h) == 0) {
-        const float p = v[i], q = v[i + h];
-        v[i] = __fadd_rn(p, q);
-        v[i + h] = __fsub_rn(p, q);
+        const float2 s = add2(P[i], P[i + h]);
+        const float2 d = sub2(P[i], P[i + h]);
+        P[i] = s;
+        P[i + h] = d;
       }
     }
   }
 }
 
-// Offset (in floats) of element (a, b) of a block inside its slot region.
-// Row a is 16 floats; its four 16-byte units are XOR-permuted by (a >> 1) & 3
-// so that the float4 writes of pass 1 and the scalar column reads of pass 2
-// are both free of bank conflicts.
-__device__ __forceinline__ int swz(int a, int b) {
-  return a * 16 + ((((b >> 2) ^ (a >> 1)) & 3) << 2) + (b & 3);
-}
-
-// Rotates one block: `v` holds this thread's pass-1 row (a = lane16) on entry
-// and its pass-2 column (b = lane16) on exit, scaled by 1/16.  `slot_smem` is
-// the half-warp's private region.  Must be called by all 32 lanes of the warp
-// (`active` masks the work, not the barriers).
-__device__ __forceinline__ void rotate_block(float (&v)[16], float* slot_smem, int lane16,
-                                             bool active) {
-  if (active) {
-    fwht16(v);
+// 8-point transform over the array index of pairs.
+__device__ __forceinline__ void fwht8x2(float2 (&P)[8]) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float4 w = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-      *reinterpret_cast<float4*>(slot_smem + swz(lane16, 4 * u)) = w;
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const float2 s = add2(P[i], P[i + h]);
+        const float2 d = sub2(P[i], P[i + h]);
+        P[i] = s;
+        P[i + h] = d;
+      }
     }
   }
-  __syncwarp();
+}
+
+// Block state after pass 2: U[p] = (z[2p][2q], z[2p+1][2q]),
+// V[p] = (z[2p][2q+1], z[2p+1][2q+1]).
+struct BlockCols {
+  float2 U[8], V[8];
+};
+
+// Pass 1 (on P, in place), transpose through `slot_smem`, pass 2 into `out`.
+// Must be reached by every lane of the warp (`active` masks the work only).
+__device__ __forceinline__ void rotate_block(float2 (&P)[16], BlockCols& out, char* slot_smem,
+                                             int lane8, bool active) {
   if (active) {
+    fwht16x2(P);
+    // unit (p, b) at p * 18 + b; thread p writes its 16 units as 8 x 16 bytes
+    float4* wrow = reinterpret_cast<float4*>(slot_smem + lane8 * kRowUnits * 8);
 #pragma unroll
-    for (int a = 0; a < 16; ++a) v[a] = slot_smem[swz(a, lane16)];
-    fwht16(v);
-#pragma unroll
-    for (int a = 0; a < 16; ++a) v[a] = v[a] * 0.0625f;   // exact: power of two
+    for (int b = 0; b < 16; b += 2) wrow[b / 2] = make_float4(P[b].x, P[b].y, P[b + 1].x, P[b + 1].y);
   }
   __syncwarp();
+  if (active) {
+    const char* rbase = slot_smem + 2 * lane8 * 8;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const float4 w = *reinterpret_cast<const float4*>(rbase + p * kRowUnits * 8);
+      // scalar stage over s (a = 2p + s)
+      out.U[p] = make_float2(w.x + w.y, w.x - w.y);
+      out.V[p] = make_float2(w.z + w.w, w.z - w.w);
+    }
+    fwht8x2(out.U);
+    fwht8x2(out.V);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ float absmax_cols(float m, const BlockCols& c) {
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    m = fmaxf(m, fmaxf(fabsf(c.U[p].x), fabsf(c.U[p].y)));
+    m = fmaxf(m, fmaxf(fabsf(c.V[p].x), fabsf(c.V[p].y)));
+  }
+  return m;
+}
+
+__device__ __forceinline__ void scale_cols(BlockCols& c, float f) {
+  const float2 ff = make_float2(f, f);
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    c.U[p] = mul2(c.U[p], ff);
+    c.V[p] = mul2(c.V[p], ff);
+  }
 }
 
 // Row absmax over the CTA.  `red` holds one float per warp.
@@ -82,8 +157,11 @@ __device__ __forceinline__ float cta_absmax(float local, float* red) {
   return m;
 }
 
-// FP32 quantiser shared by both operands: s = fp32(amax / 127),
-// r = fp32(1 / s), code = clamp(rint(fp32(v * r)), -127, 127).
+// FP32 quantiser shared by both operands, for a row of rotated values v:
+// s = fp32(amax / 127), r = fp32(1 / s), code = rint(fp32(v * r)) (half to
+// even).  |v| <= amax bounds |v * r| by 127 * (1 + 3 * 2^-24), so the code
+// never leaves [-127, 127].  Degenerate rows (s == 0 or r overflowing) get
+// s = 0 and all-zero codes.
 struct RowQuant {
   float s, r;
   bool degenerate;
@@ -91,29 +169,40 @@ struct RowQuant {
     s = __fdiv_rn(amax, 127.0f);
     r = __frcp_rn(s);
     degenerate = (s == 0.0f) || isinf(r);
-    if (degenerate) s = 0.0f;
-  }
-  __device__ __forceinline__ int code(float v) const {
-    if (degenerate) return 0;
-    int q = __float2int_rn(__fmul_rn(v, r));
-    return max(-127, min(127, q));
+    if (degenerate) {
+      s = 0.0f;
+      r = 0.0f;
+    }
   }
 };
 
-// Writes the 16 codes of this thread's pass-2 column of block `blk`:
-// element 16 a + lane16 for a = 0..15.  For each a the 16 threads of a slot
-// cover 16 consecutive codes.
-__device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk, int lane16,
-                                            const float (&v)[16], const RowQuant& rq) {
-  const int base = blk * kBlock + lane16;
+__device__ __forceinline__ float rint_f(float v) {
+  float d;
+  asm("cvt.rni.f32.f32 %0, %1;" : "=f"(d) : "f"(v));
+  return d;
+}
+
+// Writes the codes of one block: values (already multiplied by r, so only
+// the rounding is left) for rows 2p, 2p+1 and columns 2q, 2q+1.
+__device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk, int lane8,
+                                            const BlockCols& c) {
+  const int col = blk * kBlock + 2 * lane8;
   if (f16_codes) {
-    __half* q = static_cast<__half*>(q_row) + base;
+    __half2* q = reinterpret_cast<__half2*>(static_cast<__half*>(q_row) + col);
 #pragma unroll
-    for (int a = 0; a < 16; ++a) q[16 * a] = __int2half_rn(rq.code(v[a]));
+    for (int p = 0; p < 8; ++p) {
+      q[(32 * p) / 2] = __floats2half2_rn(rint_f(c.U[p].x), rint_f(c.V[p].x));        // row 2p
+      q[(32 * p + 16) / 2] = __floats2half2_rn(rint_f(c.U[p].y), rint_f(c.V[p].y));   // row 2p+1
+    }
   } else {
-    int8_t* q = static_cast<int8_t*>(q_row) + base;
+    uint16_t* q = reinterpret_cast<uint16_t*>(static_cast<int8_t*>(q_row) + col);
 #pragma unroll
-    for (int a = 0; a < 16; ++a) q[16 * a] = static_cast<int8_t>(rq.code(v[a]));
+    for (int p = 0; p < 8; ++p) {
+      const int a0 = __float2int_rn(c.U[p].x), b0 = __float2int_rn(c.V[p].x);
+      const int a1 = __float2int_rn(c.U[p].y), b1 = __float2int_rn(c.V[p].y);
+      q[(32 * p) / 2] = static_cast<uint16_t>((a0 & 0xff) | ((b0 & 0xff) << 8));
+      q[(32 * p + 16) / 2] = static_cast<uint16_t>((a1 & 0xff) | ((b1 & 0xff) << 8));
+    }
   }
 }
 

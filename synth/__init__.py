@@ -135,6 +135,18 @@ def _nearest_code(v: np.ndarray, grid: np.ndarray) -> np.ndarray:
     return np.where(pick_hi, hi, lo).astype(np.uint8)
 
 
+def _nearest_e2m1(v: np.ndarray) -> np.ndarray:
+    """Nearest E2M1 magnitude code of v >= 0 (same rule as _nearest_code, ties to
+    the even code), by counting the midpoints of the grid that v lies above."""
+    mids = 0.5 * (_E2M1_GRID[1:] + _E2M1_GRID[:-1])
+    code = np.zeros(v.shape, dtype=np.uint8)
+    for i, m in enumerate(mids):
+        m = np.float32(m)
+        # a tie goes up when the upper neighbour (code i+1) is even
+        code += (v >= m) if (i + 1) % 2 == 0 else (v > m)
+    return code
+
+
 def make_nvfp4_weight(wl: Workload, rows: int | None = None, std: float = 0.02,
                       row_chunk: int = 2048):
     """Weights W [N, K] ~ N(0, std) stored as NVFP4.
@@ -163,7 +175,7 @@ def make_nvfp4_weight(wl: Workload, rows: int | None = None, std: float = 0.02,
         sval = _E4M3_GRID[sc] * float(t)
         with np.errstate(divide="ignore", invalid="ignore"):
             v = np.where(sval[..., None] > 0, blk / sval[..., None], 0.0)
-        mag = _nearest_code(np.abs(v), _E2M1_GRID)
+        mag = _nearest_e2m1(np.abs(v).astype(np.float32))
         nib = np.where((v < 0) & (mag > 0), mag | 8, mag).astype(np.uint8)
         nib = nib.reshape(r1 - r0, Ks)
         packed[r0:r1] = nib[:, 0::2] | (nib[:, 1::2] << 4)
