@@ -155,6 +155,14 @@ int convrot_gemm_i32(const void* a_q, int64_t ld_aq,
                      int32_t* acc, int64_t ld_acc, cudaStream_t stream);
 
 /*
+ * Text of the last CUDA error that made a call of this library return
+ * CONVROT_ERR_CUDA in the calling thread, naming the failing CUDA call
+ * ("" if none).  The string is owned by the library and stays valid until
+ * the thread's next failing call.
+ */
+const char* convrot_last_error(void);
+
+/*
  * Device-side failure report.  Kernels that wait on asynchronous copies or
  * tensor-core work give up after about two seconds, record a nonzero code in
  * a device word and return early (their outputs are then incomplete).  This

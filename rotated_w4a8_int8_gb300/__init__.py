@@ -13,7 +13,7 @@ import ctypes
 import os
 
 __all__ = [
-    "load_library", "padded_k", "status_string", "prepare_weight", "quant_act", "gemm",
+    "load_library", "padded_k", "status_string", "last_error", "prepare_weight", "quant_act", "gemm",
     "gemm_i32", "device_error", "ConvRotError", "BF16", "FP16", "FP32", "CODES_S8",
     "CODES_F16", "LIB_PATH", "EXPORTS",
 ]
@@ -22,14 +22,17 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libconvrot.
 BF16, FP16, FP32 = 0, 1, 2
 CODES_S8, CODES_F16 = 0, 1
 EXPORTS = ("convrot_padded_k", "convrot_status_string", "convrot_prepare_weight",
-           "convrot_quant_act", "convrot_gemm", "convrot_gemm_i32", "convrot_device_error")
+           "convrot_quant_act", "convrot_gemm", "convrot_gemm_i32", "convrot_device_error",
+           "convrot_last_error")
 
 _lib = None
 
 
 class ConvRotError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+        detail = last_error() if status == 4 else ""
+        msg = f"{fn} failed: {status_string(status)} (status {status})"
+        super().__init__(msg + (f": {detail}" if detail else ""))
         self.status = status
 
 
@@ -54,6 +57,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.convrot_gemm.restype = i32
     lib.convrot_gemm_i32.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp, i64, vp]
     lib.convrot_gemm_i32.restype = i32
+    lib.convrot_last_error.argtypes = []
+    lib.convrot_last_error.restype = ctypes.c_char_p
     lib.convrot_device_error.argtypes = [vp, ctypes.POINTER(i32)]
     lib.convrot_device_error.restype = i32
     del f
@@ -67,6 +72,11 @@ def padded_k(K: int) -> int:
 
 def status_string(status: int) -> str:
     return load_library().convrot_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    """Text of the CUDA error behind the calling thread's last CONVROT_ERR_CUDA."""
+    return load_library().convrot_last_error().decode()
 
 
 def _ptr(t) -> int:

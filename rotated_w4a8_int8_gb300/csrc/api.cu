@@ -1,5 +1,24 @@
 // Host-only helpers of the ConvRot C ABI.
+#include <cstdio>
+
 #include "../../include/convrot.h"
+#include "errors.h"
+
+static thread_local char g_last_error[256] = "";
+
+namespace convrot {
+int record_cuda_error(const char* what, cudaError_t e) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorString(e),
+                cudaGetErrorName(e));
+  return CONVROT_ERR_CUDA;
+}
+int record_error(const char* what) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+  return CONVROT_ERR_CUDA;
+}
+}  // namespace convrot
+
+extern "C" const char* convrot_last_error(void) { return g_last_error; }
 
 extern "C" int convrot_padded_k(int K) {
   if (K <= 0) return 0;

@@ -20,19 +20,25 @@
 // registers while the tensor core fills the other buffer.
 //
 // CTA tile 128 x 256 (UMMA M=128, N=256, K=16), K step 64 (one 128-byte
-// swizzled row per operand row), 4-stage TMA ring, persistent CTAs over a
-// grouped tile order.  Warp 0: TMA producer.  Warp 1: TMEM owner and MMA
-// issuer.  Warps 2..9: epilogue.  Every mbarrier wait is bounded: after about
-// two seconds the waiting role records an error code, the CTA drains what it
-// has in flight and returns.
+// swizzled row per operand row), 4-stage TMA ring.  CTAs run in clusters of
+// two that own vertically adjacent M tiles of the same N tile: each CTA
+// loads its own A tile and one half of the shared B tile, multicast into both
+// CTAs, so every SM pulls 32 KiB instead of 48 KiB from L2 per K step.  A
+// stage is refilled only after the MMAs of both CTAs have released it.
+// Clusters are persistent over a grouped tile order.  Warp 0: TMA producer.
+// Warp 1: TMEM owner and MMA issuer.  Warps 2..9: epilogue.  Every mbarrier
+// wait is bounded: after about two seconds the waiting role records an error
+// code, the CTA drains what it has in flight and returns.
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "../../include/convrot.h"
+#include "errors.h"
 
 namespace crgemm {
 
@@ -45,8 +51,16 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32; // 320
 constexpr int TMEM_COLS = 512;                   // two 256-column FP32 buffers
-constexpr int GROUP_M = 16;                      // tile raster: 16 M-tiles share each B tile
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int CLUSTER = 2;                       // CTAs sharing one B tile (adjacent M tiles)
+constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;  // part of B each CTA loads and multicasts
+constexpr int GROUP_M = 8;                       // tile raster: 8 M-tile pairs share each B tile
+// Output staging: each epilogue warp writes its 32 rows x 128 columns as
+// boxes of 32 rows x 64 bytes (64-byte swizzle), two buffers per warp, and
+// hands every box to a TMA tensor store.
+constexpr int OUT_BOX_BYTES = 64;
+constexpr int OUT_BOX = 32 * OUT_BOX_BYTES;                  // 2 KiB
+constexpr int OUT_STAGING = NUM_EPI_WARPS * 2 * OUT_BOX;     // 32 KiB
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 enum ErrCode : int { ERR_NONE = 0, ERR_WAIT_FULL = 1, ERR_WAIT_EMPTY = 2, ERR_WAIT_ACC_FULL = 3,
@@ -118,6 +132,42 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Same as tma_load_2d, but the tile lands at the same shared-memory offset
+// in every CTA of `mask` and completes the mbarrier at that offset in each.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int x, int y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+      " [%0], [%1, {%3, %4}], [%2], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
+      : "memory");
+}
+
+// TMA tensor store of one box from shared memory; completion is tracked
+// per thread with bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs; the barrier instructions are warp-aligned.
+__device__ __forceinline__ void cluster_sync() {
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -128,6 +178,14 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                ::"r"(bar) : "memory");
+}
+
+// Arrive on the mbarrier at this offset in every CTA of `mask` once all
+// previously issued tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(bar), "h"(mask) : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, FP16 inputs, FP32 accumulate.
@@ -184,14 +242,18 @@ constexpr uint32_t kIdesc = (1u << 4)                         // D format: F32
 
 struct Params {
   int M, N, K_p;
-  int num_m, num_n, num_tiles, k_steps;
+  int num_m, num_n, k_steps;
+  int num_mp, num_pair_tiles;     // M-tile pairs (one per cluster) and pair tiles
   const float* a_scale;
   const float* w_scale;
   void* out;
   int64_t ld_out;
   int out_vec;      // 16-byte vector stores allowed (base and pitch aligned)
+  int out_tma;      // output written by TMA tensor stores (base and pitch 16-byte aligned)
 };
 
+// Pair tile -> (M-tile pair, N tile), grouped so that GROUP_M pairs in a row
+// reuse each B tile from L2.
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
   const int per_group = GROUP_M * num_n;
   const int g = tile / per_group;
@@ -219,10 +281,11 @@ template <> __device__ __forceinline__ float to_out<CONVROT_FP32>(float y) { ret
 template <int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-            const Params p) {
+            const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + OUT_STAGING);
   // barrier slots: full[4], empty[4], acc_full[2], acc_empty[2], drain
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
@@ -235,7 +298,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CLUSTER);      // released by the MMAs of both CTAs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
@@ -257,8 +320,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  // the peer's multicasts and commits target our barriers: both CTAs must
+  // have initialised theirs before either issues anything
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int rank = static_cast<int>(cluster_rank());
+  const int cluster_id = blockIdx.x / CLUSTER, num_clusters = gridDim.x / CLUSTER;
+  constexpr uint16_t kPeers = (1u << CLUSTER) - 1u;
 
   const int k_steps = p.k_steps;
   const int chunks_per_tile = (k_steps + KCHUNK_STEPS - 1) / KCHUNK_STEPS;
@@ -270,22 +339,33 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       uint32_t phase = 0;
       bool ok = true;
       uint32_t issued_mask = 0, issued_phase = 0;   // last outstanding load per stage
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, p.num_m, p.num_n, mb, nb);
+      for (int tile = cluster_id; tile < p.num_pair_tiles && ok; tile += num_clusters) {
+        int mp, nb;
+        tile_coords(tile, p.num_mp, p.num_n, mp, nb);
+        const int mb = mp * CLUSTER + rank;
         for (int ks = 0; ks < k_steps; ++ks) {
+          // the stage is free once the MMAs of BOTH CTAs have consumed it
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, ERR_WAIT_EMPTY, abort_flag)) { ok = false; break; }
           const uint32_t fb = full0 + 8 * stage;
+          // own A tile + both halves of B (ours and the peer's multicast)
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           tma_load_2d(sa, &tmap_a, fb, ks * BK, mb * BM);
-          tma_load_2d(sa + A_BYTES, &tmap_b, fb, ks * BK, nb * BN);
+          tma_load_2d_mc(sa + A_BYTES + rank * B_HALF_BYTES, &tmap_b, fb, ks * BK,
+                         nb * BN + rank * (BN / CLUSTER), kPeers);
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      if (!ok) {
+      if (ok) {
+        // the peer's MMA commits arrive on our empty barriers: wait until both
+        // CTAs have released the last use of every stage before leaving
+        for (int i = 0; i < STAGES; ++i) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, ERR_WAIT_EMPTY, abort_flag)) break;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      } else {
         // let every load still in flight land before the CTA can exit
         for (int s = 0; s < STAGES; ++s)
           if (issued_mask & (1u << s)) {
@@ -303,7 +383,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       uint32_t chunk = 0;          // running chunk counter -> TMEM buffer and its phase
       bool ok = true;
       bool any = false;
-      for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+      for (int tile = cluster_id; tile < p.num_pair_tiles && ok; tile += num_clusters) {
         for (int c = 0; c < chunks_per_tile && ok; ++c, ++chunk) {
           const uint32_t buf = chunk & 1u, use = chunk >> 1;
           if (!mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, ERR_WAIT_ACC_EMPTY, abort_flag)) { ok = false; break; }
@@ -321,7 +401,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
               tc_mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, (ks > ks0 || kk > 0) ? 1u : 0u);
             }
             any = true;
-            tc_commit(empty0 + 8 * stage);
+            tc_commit_mc(empty0 + 8 * stage, kPeers);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
           if (ok) tc_commit(accf0 + 8 * buf);
@@ -341,10 +421,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const int col_half = ew >> 2;             // columns [0,128) or [128,256) of the tile
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t chunk = 0;
+    uint32_t boxes = 0;                       // output boxes staged by this warp so far
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-      int mb, nb;
-      tile_coords(tile, p.num_m, p.num_n, mb, nb);
+    for (int tile = cluster_id; tile < p.num_pair_tiles && ok; tile += num_clusters) {
+      int mp, nb;
+      tile_coords(tile, p.num_mp, p.num_n, mp, nb);
+      const int mb = mp * CLUSTER + rank;
       int32_t acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0;
@@ -374,18 +456,64 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       }
       if (!ok) break;
       // ---- output: this thread owns row m, columns n0 .. n0+127
-      const int m = mb * BM + quarter * 32 + lane;
+      const int m_base = mb * BM + quarter * 32;
+      const int m = m_base + lane;
       const int n0 = nb * BN + col_half * 128;
-      if (m < p.M) {
-        if constexpr (OUT < 0) {
+      if constexpr (OUT < 0) {
+        if (m < p.M) {
           int32_t* orow = static_cast<int32_t*>(p.out) + static_cast<int64_t>(m) * p.ld_out;
 #pragma unroll
           for (int j = 0; j < 128; ++j)
             if (n0 + j < p.N) orow[n0 + j] = acc[j];
-        } else {
-          using T = typename OutT<OUT>::T;
-          constexpr int VEC = 16 / sizeof(T);
-          const float sa = __ldg(p.a_scale + m);
+        }
+      } else {
+        using T = typename OutT<OUT>::T;
+        constexpr int VEC = 16 / sizeof(T);           // outputs per 16-byte chunk
+        const float sa = (m < p.M) ? __ldg(p.a_scale + m) : 0.f;
+        if (p.out_tma) {
+          constexpr int CPB = OUT_BOX_BYTES / sizeof(T);   // columns per box
+          uint8_t* wstage = staging + ew * 2 * OUT_BOX;
+#pragma unroll
+          for (int b = 0; b < 128 / CPB; ++b) {
+            const int buf = static_cast<int>(boxes & 1u);
+            if (boxes >= 2) {
+              // the store issued from this buffer two boxes ago must have read it
+              if (lane == 0) bulk_wait_read_1();
+              __syncwarp();
+            }
+            ++boxes;
+            uint8_t* rowp = wstage + buf * OUT_BOX + lane * OUT_BOX_BYTES;
+#pragma unroll
+            for (int c = 0; c < OUT_BOX_BYTES / 16; ++c) {
+              const int j0 = b * CPB + c * VEC;            // first column of this chunk
+              const int n = n0 + j0;
+              float sw[VEC];
+              if (n + VEC <= p.N) {
+#pragma unroll
+                for (int q = 0; q < VEC; q += 4) {
+                  const float4 f = __ldg(reinterpret_cast<const float4*>(p.w_scale + n + q));
+                  sw[q] = f.x; sw[q + 1] = f.y; sw[q + 2] = f.z; sw[q + 3] = f.w;
+                }
+              } else {
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) sw[q] = (n + q < p.N) ? __ldg(p.w_scale + n + q) : 0.f;
+              }
+              union { T v[VEC]; uint4 u; } pk;
+#pragma unroll
+              for (int q = 0; q < VEC; ++q)
+                pk.v[q] = to_out<OUT>(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + q]), sa), sw[q]));
+              // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
+              *reinterpret_cast<uint4*>(rowp + ((c ^ ((lane >> 1) & 3)) << 4)) = pk.u;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            // boxes wholly outside the matrix (M or N tail) are not stored
+            if (lane == 0 && m_base < p.M && n0 + b * CPB < p.N) {
+              tma_store_2d(&tmap_out, smem_u32(wstage + buf * OUT_BOX), n0 + b * CPB, m_base);
+              bulk_commit();
+            }
+          }
+        } else if (m < p.M) {
           T* orow = static_cast<T*>(p.out) + static_cast<int64_t>(m) * p.ld_out;
 #pragma unroll
           for (int j0 = 0; j0 < 128; j0 += VEC) {
@@ -413,10 +541,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
       }
     }
+    // every TMA store of this warp must be complete before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();            // neither CTA leaves while its peer may still write into it
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
@@ -444,6 +576,24 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Store map over the output [M][N] (pitch ld_out elements): boxes of 32 rows x
+// 64 bytes with 64-byte swizzle; TMA clips the parts outside the matrix.
+static bool make_out_map(CUtensorMap* map, void* base, int out_kind, int M, int N, int64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const size_t es = out_kind == CONVROT_FP32 ? 4 : 2;
+  const CUtensorMapDataType dt = out_kind == CONVROT_FP32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : out_kind == CONVROT_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(OUT_BOX_BYTES / es), 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D map over an FP16 [rows][cols] matrix with pitch ld (elements), box
 // [box_rows][64], 128-byte swizzle, zero fill outside the matrix.
 static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int64_t ld, int box_rows) {
@@ -459,25 +609,42 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int
   return r == CUDA_SUCCESS;
 }
 
-static int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
-
+// Persistent grid: as many clusters as can be resident at once (one CTA per
+// SM), never more than there are pair tiles.
 template <int OUT>
-static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const Params& p, int grid,
-                          cudaStream_t st) {
-  static bool attr_set = false;   // per-process; same attribute value on every device
-  if (!attr_set) {
+static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
+                          const Params& p, cudaStream_t st) {
+  static int max_clusters = 0;   // per process and instantiation; one device per process
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    cfg.gridDim = dim3(sms / CLUSTER * CLUSTER);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<OUT>, &cfg);
+    if (e != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = sms / CLUSTER;
+    }
+    max_clusters = n;
   }
-  gemm_kernel<OUT><<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, p);
-  return cudaGetLastError();
+  const int clusters = p.num_pair_tiles < max_clusters ? p.num_pair_tiles : max_clusters;
+  cfg.gridDim = dim3(clusters * CLUSTER);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<OUT>, ma, mb, mo, p);
 }
 
 static int validate_operands(const void* a_q, int64_t ld_aq, const void* w_q, int64_t ld_wq, int M,
@@ -502,7 +669,8 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.K_p = K_p;
   p.num_m = (M + BM - 1) / BM;
   p.num_n = (N + BN - 1) / BN;
-  p.num_tiles = p.num_m * p.num_n;
+  p.num_mp = (p.num_m + CLUSTER - 1) / CLUSTER;
+  p.num_pair_tiles = p.num_mp * p.num_n;
   p.k_steps = K_p / BK;
   p.a_scale = a_scale;
   p.w_scale = w_scale;
@@ -510,19 +678,20 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.ld_out = ld_out;
   p.out_vec = (reinterpret_cast<uintptr_t>(out) % 16 == 0) && ((ld_out * static_cast<int64_t>(out_esize)) % 16 == 0);
   CUtensorMap ma, mb;
-  if (!make_map(&ma, a_q, M, K_p, ld_aq, BM) || !make_map(&mb, w_q, N, K_p, ld_wq, BN))
-    return CONVROT_ERR_CUDA;
-  const int sms = sm_count();
-  if (sms <= 0) return CONVROT_ERR_CUDA;
-  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  if (!make_map(&ma, a_q, M, K_p, ld_aq, BM) || !make_map(&mb, w_q, N, K_p, ld_wq, BN / CLUSTER))
+    return convrot::record_error("cuTensorMapEncodeTiled failed for an operand map");
+  CUtensorMap mo;
+  memset(&mo, 0, sizeof(mo));
+  p.out_tma = 0;
+  if (out_kind >= 0 && p.out_vec) p.out_tma = make_out_map(&mo, out, out_kind, M, N, ld_out) ? 1 : 0;
   cudaError_t e;
   switch (out_kind) {
-    case CONVROT_BF16: e = launch<CONVROT_BF16>(ma, mb, p, grid, stream); break;
-    case CONVROT_FP16: e = launch<CONVROT_FP16>(ma, mb, p, grid, stream); break;
-    case CONVROT_FP32: e = launch<CONVROT_FP32>(ma, mb, p, grid, stream); break;
-    default: e = launch<-1>(ma, mb, p, grid, stream); break;
+    case CONVROT_BF16: e = launch<CONVROT_BF16>(ma, mb, mo, p, stream); break;
+    case CONVROT_FP16: e = launch<CONVROT_FP16>(ma, mb, mo, p, stream); break;
+    case CONVROT_FP32: e = launch<CONVROT_FP32>(ma, mb, mo, p, stream); break;
+    default: e = launch<-1>(ma, mb, mo, p, stream); break;
   }
-  return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
+  return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("GEMM launch", e);
 }
 
 }  // namespace crgemm
@@ -558,12 +727,15 @@ extern "C" int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const void* w_q,
 }
 
 extern "C" int convrot_device_error(cudaStream_t stream, int* code) {
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return CONVROT_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return convrot::record_cuda_error("cudaStreamSynchronize", e);
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_error, sizeof(int)) != cudaSuccess) return CONVROT_ERR_CUDA;
+  e = cudaMemcpyFromSymbol(&v, g_error, sizeof(int));
+  if (e != cudaSuccess) return convrot::record_cuda_error("reading the device error word", e);
   if (v != 0) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_error, &zero, sizeof(int)) != cudaSuccess) return CONVROT_ERR_CUDA;
+    e = cudaMemcpyToSymbol(g_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return convrot::record_cuda_error("clearing the device error word", e);
   }
   if (code) *code = v;
   return v ? CONVROT_ERR_DEVICE_TIMEOUT : CONVROT_OK;

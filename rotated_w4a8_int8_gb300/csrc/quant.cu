@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 
 #include "../../include/convrot.h"
+#include "errors.h"
 #include "rotate_quant.cuh"
 
 namespace convrot {
@@ -362,7 +363,7 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
     case CONVROT_FP16: e = launch_act<DT_FP16>(g, M, x, ld_x, K, swiglu != 0, vec, a_q, f16, ld_aq, a_scale, stream); break;
     default: e = launch_act<DT_FP32>(g, M, x, ld_x, K, swiglu != 0, vec, a_q, f16, ld_aq, a_scale, stream); break;
   }
-  return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
+  return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("quant_act launch", e);
 }
 
 extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
@@ -391,5 +392,5 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
     case 2: e = launch_weight_nb<2>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
     default: e = launch_weight_nb<4>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
   }
-  return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA;
+  return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("prepare_weight launch", e);
 }
