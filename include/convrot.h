@@ -155,6 +155,19 @@ int convrot_gemm_i32(const void* a_q, int64_t ld_aq,
                      int32_t* acc, int64_t ld_acc, cudaStream_t stream);
 
 /*
+ * Failure-detection self-test: launches the GEMM of convrot_gemm_i32 on the
+ * given operands with its TMA producer switched off, so the first wait for
+ * operand tiles runs out (after about two seconds).  The kernel then records
+ * the failure, drains and returns; acc is left incomplete.  Afterwards
+ * convrot_device_error reports CONVROT_ERR_DEVICE_TIMEOUT with a nonzero
+ * code, and the CUDA context stays usable.  Returns the launch status.
+ */
+int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq,
+                                  const void* w_q, int64_t ld_wq,
+                                  int M, int N, int K_p,
+                                  int32_t* acc, int64_t ld_acc, cudaStream_t stream);
+
+/*
  * Text of the last CUDA error that made a call of this library return
  * CONVROT_ERR_CUDA in the calling thread, naming the failing CUDA call
  * ("" if none).  The string is owned by the library and stays valid until

@@ -250,6 +250,7 @@ struct Params {
   int64_t ld_out;
   int out_vec;      // 16-byte vector stores allowed (base and pitch aligned)
   int out_tma;      // output written by TMA tensor stores (base and pitch 16-byte aligned)
+  int test_stall;   // failure-detection self-test: the producer issues no loads
 };
 
 // Pair tile -> (M-tile pair, N tile), grouped so that GROUP_M pairs in a row
@@ -339,7 +340,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       uint32_t phase = 0;
       bool ok = true;
       uint32_t issued_mask = 0, issued_phase = 0;   // last outstanding load per stage
-      for (int tile = cluster_id; tile < p.num_pair_tiles && ok; tile += num_clusters) {
+      for (int tile = cluster_id; tile < p.num_pair_tiles && ok && !p.test_stall; tile += num_clusters) {
         int mp, nb;
         tile_coords(tile, p.num_mp, p.num_n, mp, nb);
         const int mb = mp * CLUSTER + rank;
@@ -662,8 +663,9 @@ static int validate_operands(const void* a_q, int64_t ld_aq, const void* w_q, in
 
 static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scale, const void* w_q,
                int64_t ld_wq, const float* w_scale, int M, int N, int K_p, void* out, int64_t ld_out,
-               size_t out_esize, cudaStream_t stream) {
+               size_t out_esize, cudaStream_t stream, int test_stall = 0) {
   Params p;
+  p.test_stall = test_stall;
   p.M = M;
   p.N = N;
   p.K_p = K_p;
@@ -724,6 +726,16 @@ extern "C" int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const void* w_q,
   if (!acc) return CONVROT_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(acc) % 4) return CONVROT_ERR_MISALIGNED;
   return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, M, N, K_p, acc, ld_acc, 4, stream);
+}
+
+extern "C" int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, const void* w_q,
+                                             int64_t ld_wq, int M, int N, int K_p, int32_t* acc,
+                                             int64_t ld_acc, cudaStream_t stream) {
+  int st = validate_operands(a_q, ld_aq, w_q, ld_wq, M, N, K_p);
+  if (st != CONVROT_OK) return st;
+  if (M == 0 || N == 0 || !acc || ld_acc < N) return CONVROT_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(acc) % 4) return CONVROT_ERR_MISALIGNED;
+  return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, M, N, K_p, acc, ld_acc, 4, stream, 1);
 }
 
 extern "C" int convrot_device_error(cudaStream_t stream, int* code) {
