@@ -37,20 +37,34 @@ __device__ __forceinline__ uint32_t load_elem_bits(const char* row, int k) {
   else return reinterpret_cast<const uint16_t*>(row)[k];
 }
 
-template <int DT, bool VEC>
+// 32-byte read-only load (one full sector per thread).
+__device__ __forceinline__ void ldg32B(const void* p, uint32_t* w) {
+  asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+      : "l"(p));
+}
+
+// VEC: 0 = element loads, 1 = 16-byte loads, 2 = 32-byte loads (rows aligned
+// to that size; a thread's 32 elements are contiguous).
+template <int DT, int VEC>
 __device__ __forceinline__ void load_raw(const char* row, int c0, int K, Raw<DT>& r) {
   if (c0 >= K) {
 #pragma unroll
     for (int i = 0; i < Raw<DT>::N; ++i) r.w[i] = 0u;
     return;
   }
-  if (VEC && c0 + 32 <= K) {
+  if (VEC > 0 && c0 + 32 <= K) {
     constexpr int esz = (DT == DT_FP32) ? 4 : 2;
-    const uint4* p = reinterpret_cast<const uint4*>(row + static_cast<size_t>(c0) * esz);
+    const char* p = row + static_cast<size_t>(c0) * esz;
+    if constexpr (VEC == 2) {
 #pragma unroll
-    for (int u = 0; u < Raw<DT>::N / 4; ++u) {
-      const uint4 v = __ldg(p + u);
-      r.w[4 * u] = v.x; r.w[4 * u + 1] = v.y; r.w[4 * u + 2] = v.z; r.w[4 * u + 3] = v.w;
+      for (int u = 0; u < Raw<DT>::N / 8; ++u) ldg32B(p + 32 * u, &r.w[8 * u]);
+    } else {
+#pragma unroll
+      for (int u = 0; u < Raw<DT>::N / 4; ++u) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(p) + u);
+        r.w[4 * u] = v.x; r.w[4 * u + 1] = v.y; r.w[4 * u + 2] = v.z; r.w[4 * u + 3] = v.w;
+      }
     }
     return;
   }
@@ -88,17 +102,18 @@ __device__ __forceinline__ void pairs_from_raw(const Raw<DT>& r, float2 (&P)[16]
   for (int b = 0; b < 16; ++b) P[b] = make_float2(raw_elem<DT>(r, b), raw_elem<DT>(r, 16 + b));
 }
 
-// SwiGLU h = g * sigmoid(g) * v in FP32 (no intermediate rounding to the input dtype).
-__device__ __forceinline__ float swiglu1(float g, float v) {
-  return __fdividef(g, 1.0f + expf(-g)) * v;
-}
-
+// SwiGLU h = g * sigmoid(g) * v in FP32 (no intermediate rounding to the input
+// dtype): h = (g / (1 + exp(-g))) * v.
 template <int DT>
 __device__ __forceinline__ void pairs_swiglu(const Raw<DT>& g, const Raw<DT>& v, float2 (&P)[16]) {
 #pragma unroll
-  for (int b = 0; b < 16; ++b)
-    P[b] = make_float2(swiglu1(raw_elem<DT>(g, b), raw_elem<DT>(v, b)),
-                       swiglu1(raw_elem<DT>(g, 16 + b), raw_elem<DT>(v, 16 + b)));
+  for (int b = 0; b < 16; ++b) {
+    const float2 gg = make_float2(raw_elem<DT>(g, b), raw_elem<DT>(g, 16 + b));
+    const float2 vv = make_float2(raw_elem<DT>(v, b), raw_elem<DT>(v, 16 + b));
+    // h = (g / (1 + exp(-g))) * v, the two elements of the pair at once
+    const float2 d = add2(make_float2(1.0f, 1.0f), make_float2(expf(-gg.x), expf(-gg.y)));
+    P[b] = mul2(make_float2(__fdividef(gg.x, d.x), __fdividef(gg.y, d.y)), vv);
+  }
 }
 
 // NVFP4: two E2M1 codes (one byte, element 2j in the low nibble) -> FP16x2,
@@ -124,19 +139,8 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
 // Pass-1 pairs of a weight block chunk: the 32 decoded NVFP4 elements
 // [c0, c0 + 32) WITHOUT the tensor scale, u = E2M1 * E4M3 (exact in FP32);
 // elements >= K are zero (serialised padding is ignored).
-__device__ __forceinline__ void load_pairs_nvfp4(const uint8_t* prow, const uint8_t* srow, int c0,
-                                                 int K, int K_s, float2 (&P)[16]) {
-  if (c0 >= K) {
-#pragma unroll
-    for (int b = 0; b < 16; ++b) P[b] = make_float2(0.f, 0.f);
-    return;
-  }
-  const bool second = c0 + 16 < K_s;          // elements c0+16.. are stored
-  const uint2 w0 = __ldg(reinterpret_cast<const uint2*>(prow + (c0 >> 1)));
-  const uint2 w1 = second ? __ldg(reinterpret_cast<const uint2*>(prow + (c0 >> 1) + 8)) : make_uint2(0u, 0u);
-  // scale rows are K_s/16 bytes long (odd for some K): read the two bytes separately
-  const uint16_t sc = static_cast<uint16_t>(
-      __ldg(srow + (c0 >> 4)) | (second ? static_cast<uint32_t>(__ldg(srow + (c0 >> 4) + 1)) << 8 : 0u));
+__device__ __forceinline__ void decode_nvfp4_pairs(uint2 w0, uint2 w1, uint16_t sc, int c0, int K,
+                                                   float2 (&P)[16]) {
   // scales of row 2p (elements c0..c0+15) and row 2p+1 (c0+16..c0+31)
   const float2 scl = e4m3x2_to_float2(sc);
   uint32_t h0[8], h1[8];
@@ -161,31 +165,38 @@ __device__ __forceinline__ void load_pairs_nvfp4(const uint8_t* prow, const uint
 }
 
 // ------------------------------------------------------------------ kernels
-// Kernel 2: one CTA per token row.  Slot s (threads 8s .. 8s+7) rotates
-// blocks s, s + S, s + 2S, ... (at most NBMAX).
-template <int DT, bool SWIGLU, int NBMAX, bool VEC>
-__global__ void __launch_bounds__(kMaxThreads)
-quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int K, int nblocks, int S,
-                 void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
-  extern __shared__ __align__(16) char smem[];
-  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);
-  const int row = blockIdx.x;
-  const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
-  constexpr size_t esize = (DT == DT_FP32) ? 4 : 2;
-  const char* xrow = static_cast<const char*>(x) + static_cast<size_t>(row) * ld_x * esize;
-  char* my = smem + slot * kSlotBytes;
+// Both kernels run one CTA per row.  Every load of the row is issued before
+// any arithmetic.  Slot s (threads 8s .. 8s+7) rotates blocks s, s + S,
+// s + 2S, ... (at most NBMAX) of the row.
 
-  Raw<DT> raw[NBMAX];
-  Raw<DT> rawv[SWIGLU ? NBMAX : 1];
+// Raw input of one token row for this thread: the pass-1 chunks of its blocks.
+template <int DT, bool SWIGLU, int NBMAX>
+struct ActRaw {
+  Raw<DT> g[NBMAX];
+  Raw<DT> v[SWIGLU ? NBMAX : 1];
+};
+
+template <int DT, bool SWIGLU, int NBMAX, int VEC>
+__device__ __forceinline__ void load_act_row(const char* xrow, int K, int nblocks, int S, int slot,
+                                             int lane8, ActRaw<DT, SWIGLU, NBMAX>& r) {
+  constexpr size_t esize = (DT == DT_FP32) ? 4 : 2;
 #pragma unroll
-  for (int i = 0; i < NBMAX; ++i) {          // issue every load of the row first
+  for (int i = 0; i < NBMAX; ++i) {
     const int blk = slot + S * i;
     if (slot < S && blk < nblocks) {
       const int c0 = blk * kBlock + 32 * lane8;
-      load_raw<DT, VEC>(xrow, c0, K, raw[i]);
-      if constexpr (SWIGLU) load_raw<DT, VEC>(xrow + static_cast<size_t>(K) * esize, c0, K, rawv[i]);
+      load_raw<DT, VEC>(xrow, c0, K, r.g[i]);
+      if constexpr (SWIGLU) load_raw<DT, VEC>(xrow + static_cast<size_t>(K) * esize, c0, K, r.v[i]);
     }
   }
+}
+
+// One activation row from its raw input: (SwiGLU,) rotation, CTA absmax,
+// scale and codes.  `red` is this row's reduction buffer.
+template <int DT, bool SWIGLU, int NBMAX>
+__device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, int row, int nblocks, int S,
+                                        int slot, int lane8, char* my, float* red, void* q, int f16_codes,
+                                        int64_t ld_q, float* scale) {
   BlockCols c[NBMAX];
   float amax = 0.f;
 #pragma unroll
@@ -194,8 +205,8 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int K, int nblocks, i
     const bool active = (slot < S) && (blk < nblocks);
     float2 P[16];
     if (active) {
-      if constexpr (SWIGLU) pairs_swiglu<DT>(raw[i], rawv[SWIGLU ? i : 0], P);
-      else pairs_from_raw<DT>(raw[i], P);
+      if constexpr (SWIGLU) pairs_swiglu<DT>(cur.g[i], cur.v[SWIGLU ? i : 0], P);
+      else pairs_from_raw<DT>(cur.g[i], P);
     }
     rotate_block(P, c[i], my, lane8, active);
     if (active) amax = absmax_cols(amax, c[i]);
@@ -203,9 +214,8 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int K, int nblocks, i
   // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
   const RowQuant rq(cta_absmax(amax, red) * 0.0625f);
   if (threadIdx.x == 0) scale[row] = rq.s;
-  const size_t qsize = f16_codes ? 2 : 1;
-  void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * qsize;
-  const float mult = rq.r * 0.0625f;         // fp32(z * (r / 16)) == fp32((z / 16) * r)
+  void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
+  const float mult = rq.r * 0.0625f;           // fp32(z * (r / 16)) == fp32((z / 16) * r)
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int blk = slot + S * i;
@@ -216,22 +226,76 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int K, int nblocks, i
   }
 }
 
-// Kernel 1: one CTA per weight row; same block schedule as kernel 2.
-template <int NBMAX>
+// Kernel 2: one CTA per activation row.
+template <int DT, bool SWIGLU, int NBMAX, int VEC>
 __global__ void __launch_bounds__(kMaxThreads)
-prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restrict__ w_sf,
-                      const float* __restrict__ tscale, int K, int K_s, int nblocks, int S,
-                      void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
+quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S,
+                 void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
   extern __shared__ __align__(16) char smem[];
-  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);
-  const int row = blockIdx.x;
+  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);   // per-warp maxima
   const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
+  constexpr size_t esize = (DT == DT_FP32) ? 4 : 2;
+  const int row = blockIdx.x;
+  ActRaw<DT, SWIGLU, NBMAX> cur;
+  load_act_row<DT, SWIGLU, NBMAX, VEC>(static_cast<const char*>(x) + static_cast<size_t>(row) * ld_x * esize,
+                                       K, nblocks, S, slot, lane8, cur);
+  act_row<DT, SWIGLU, NBMAX>(cur, row, nblocks, S, slot, lane8, smem + slot * kSlotBytes, red, q, f16_codes,
+                             ld_q, scale);
+}
+
+// Raw NVFP4 input of one weight row for this thread.
+template <int NBMAX>
+struct WRaw {
+  uint2 w0[NBMAX], w1[NBMAX];
+  uint16_t sc[NBMAX];
+};
+
+// Packed nibbles and the two block scales of the 32 elements [c0, c0 + 32);
+// nothing past the stored row (K_s) is read.  W16: the 16 packed bytes are
+// 16-byte aligned (row pitch K_s/2 a multiple of 16) and read at once.
+template <bool W16>
+__device__ __forceinline__ void load_nvfp4_raw(const uint8_t* prow, const uint8_t* srow, int c0,
+                                               int K, int K_s, uint2& w0, uint2& w1, uint16_t& sc) {
+  if (c0 >= K) {
+    w0 = make_uint2(0u, 0u);
+    w1 = make_uint2(0u, 0u);
+    sc = 0;
+    return;
+  }
+  const bool second = c0 + 16 < K_s;          // elements c0+16.. are stored
+  if (W16 && second) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(prow + (c0 >> 1)));
+    w0 = make_uint2(v.x, v.y);
+    w1 = make_uint2(v.z, v.w);
+  } else {
+    w0 = __ldg(reinterpret_cast<const uint2*>(prow + (c0 >> 1)));
+    w1 = second ? __ldg(reinterpret_cast<const uint2*>(prow + (c0 >> 1) + 8)) : make_uint2(0u, 0u);
+  }
+  // scale rows are K_s/16 bytes long (odd for some K): read the two bytes separately
+  sc = static_cast<uint16_t>(__ldg(srow + (c0 >> 4)) |
+                             (second ? static_cast<uint32_t>(__ldg(srow + (c0 >> 4) + 1)) << 8 : 0u));
+}
+
+template <int NBMAX, bool W16>
+__device__ __forceinline__ void load_weight_row(const uint8_t* w_fp4, const uint8_t* w_sf, int row, int K,
+                                                int K_s, int nblocks, int S, int slot, int lane8,
+                                                WRaw<NBMAX>& r) {
   const uint8_t* prow = w_fp4 + static_cast<size_t>(row) * (K_s >> 1);
   const uint8_t* srow = w_sf + static_cast<size_t>(row) * (K_s >> 4);
-  // rotated weight = fp32(z * t / 16); t / 16 is exact
-  const float t16 = __ldg(tscale) * 0.0625f;
-  char* my = smem + slot * kSlotBytes;
+#pragma unroll
+  for (int i = 0; i < NBMAX; ++i) {
+    const int blk = slot + S * i;
+    if (slot < S && blk < nblocks)
+      load_nvfp4_raw<W16>(prow, srow, blk * kBlock + 32 * lane8, K, K_s, r.w0[i], r.w1[i], r.sc[i]);
+  }
+}
 
+// One weight row from its raw input: decode, rotation, tensor scale, CTA
+// absmax, scale and codes.
+template <int NBMAX>
+__device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K, int nblocks, int S, int slot,
+                                           int lane8, float t16, char* my, float* red, void* q, int f16_codes,
+                                           int64_t ld_q, float* scale) {
   BlockCols c[NBMAX];
   float amax = 0.f;
 #pragma unroll
@@ -239,17 +303,16 @@ prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
     const int blk = slot + S * i;
     const bool active = (slot < S) && (blk < nblocks);
     float2 P[16];
-    if (active) load_pairs_nvfp4(prow, srow, blk * kBlock + 32 * lane8, K, K_s, P);
+    if (active) decode_nvfp4_pairs(r.w0[i], r.w1[i], r.sc[i], blk * kBlock + 32 * lane8, K, P);
     rotate_block(P, c[i], my, lane8, active);
     if (active) {
-      scale_cols(c[i], t16);
+      scale_cols(c[i], t16);                   // rotated weight = fp32(z * t / 16)
       amax = absmax_cols(amax, c[i]);
     }
   }
   const RowQuant rq(cta_absmax(amax, red));
   if (threadIdx.x == 0) scale[row] = rq.s;
-  const size_t qsize = f16_codes ? 2 : 1;
-  void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * qsize;
+  void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int blk = slot + S * i;
@@ -258,6 +321,23 @@ prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
       store_codes(qrow, f16_codes, blk, lane8, c[i]);
     }
   }
+}
+
+// Kernel 1: one CTA per weight row.
+template <int NBMAX, bool W16>
+__global__ void __launch_bounds__(kMaxThreads)
+prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restrict__ w_sf,
+                      const float* __restrict__ tscale, int N, int K, int K_s, int nblocks, int S,
+                      void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
+  extern __shared__ __align__(16) char smem[];
+  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);
+  const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
+  const float t16 = __ldg(tscale) * 0.0625f;  // t / 16 is exact
+  const int row = blockIdx.x;
+  WRaw<NBMAX> r0;
+  load_weight_row<NBMAX, W16>(w_fp4, w_sf, row, K, K_s, nblocks, S, slot, lane8, r0);
+  weight_row<NBMAX>(r0, row, K, nblocks, S, slot, lane8, t16, smem + slot * kSlotBytes, red, q, f16_codes,
+                    ld_q, scale);
 }
 
 // ------------------------------------------------------------------ launch geometry
@@ -285,17 +365,17 @@ static cudaError_t prep_smem(Kern k, size_t smem) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }
 
-template <int DT, bool SWIGLU, bool VEC, int NB>
+template <int DT, bool SWIGLU, int VEC, int NB>
 static cudaError_t launch_act_nb(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
                                  void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
   auto k = quant_act_kernel<DT, SWIGLU, NB, VEC>;
   cudaError_t e = prep_smem(k, g.smem);
   if (e != cudaSuccess) return e;
-  k<<<M, g.threads, g.smem, st>>>(x, ld_x, K, g.nblocks, g.S, q, f16, ld_q, scale);
+  k<<<M, g.threads, g.smem, st>>>(x, ld_x, M, K, g.nblocks, g.S, q, f16, ld_q, scale);
   return cudaGetLastError();
 }
 
-template <int DT, bool SWIGLU, bool VEC>
+template <int DT, bool SWIGLU, int VEC>
 static cudaError_t launch_act_dt(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
                                  void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
   switch (g.nbmax) {
@@ -307,25 +387,39 @@ static cudaError_t launch_act_dt(const RowGeometry& g, int M, const void* x, int
 
 template <int DT>
 static cudaError_t launch_act(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
-                              bool swiglu, bool vec, void* q, int f16, int64_t ld_q, float* scale,
+                              bool swiglu, int vec, void* q, int f16, int64_t ld_q, float* scale,
                               cudaStream_t st) {
   if (swiglu) {
-    return vec ? launch_act_dt<DT, true, true>(g, M, x, ld_x, K, q, f16, ld_q, scale, st)
-               : launch_act_dt<DT, true, false>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    switch (vec) {
+      case 2: return launch_act_dt<DT, true, 2>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+      case 1: return launch_act_dt<DT, true, 1>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+      default: return launch_act_dt<DT, true, 0>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    }
   }
-  return vec ? launch_act_dt<DT, false, true>(g, M, x, ld_x, K, q, f16, ld_q, scale, st)
-             : launch_act_dt<DT, false, false>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+  switch (vec) {
+    case 2: return launch_act_dt<DT, false, 2>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    case 1: return launch_act_dt<DT, false, 1>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    default: return launch_act_dt<DT, false, 0>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+  }
 }
 
-template <int NB>
+template <int NB, bool W16>
 static cudaError_t launch_weight_nb(const RowGeometry& g, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
                                     const float* t, int K, int K_s, void* q, int f16, int64_t ld_q,
                                     float* scale, cudaStream_t st) {
-  auto k = prepare_weight_kernel<NB>;
+  auto k = prepare_weight_kernel<NB, W16>;
   cudaError_t e = prep_smem(k, g.smem);
   if (e != cudaSuccess) return e;
-  k<<<N, g.threads, g.smem, st>>>(w_fp4, w_sf, t, K, K_s, g.nblocks, g.S, q, f16, ld_q, scale);
+  k<<<N, g.threads, g.smem, st>>>(w_fp4, w_sf, t, N, K, K_s, g.nblocks, g.S, q, f16, ld_q, scale);
   return cudaGetLastError();
+}
+
+template <int NB>
+static cudaError_t launch_weight_w(const RowGeometry& g, bool w16, int N, const uint8_t* w_fp4,
+                                   const uint8_t* w_sf, const float* t, int K, int K_s, void* q, int f16,
+                                   int64_t ld_q, float* scale, cudaStream_t st) {
+  return w16 ? launch_weight_nb<NB, true>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st)
+             : launch_weight_nb<NB, false>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
 }
 
 }  // namespace convrot
@@ -350,10 +444,12 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
   if (reinterpret_cast<uintptr_t>(a_q) % (fmt == CONVROT_CODES_F16 ? 4 : 2) || ld_aq % 2)
     return CONVROT_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(a_scale) % 4) return CONVROT_ERR_MISALIGNED;
-  // vector path: every row start and the value half (SwiGLU) 16-byte aligned
-  const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
-                   ((ld_x * static_cast<int64_t>(esize)) % 16 == 0) &&
-                   (!swiglu || (static_cast<int64_t>(K) * esize) % 16 == 0);
+  // vector paths: every row start and the value half (SwiGLU) aligned to 32 or 16 bytes
+  auto aligned = [&](int64_t a) {
+    return (reinterpret_cast<uintptr_t>(x) % a == 0) && ((ld_x * static_cast<int64_t>(esize)) % a == 0) &&
+           (!swiglu || (static_cast<int64_t>(K) * esize) % a == 0);
+  };
+  const int vec = aligned(32) ? 2 : aligned(16) ? 1 : 0;
   RowGeometry g;
   if (!row_geometry(K_p, &g)) return CONVROT_ERR_UNSUPPORTED;
   const int f16 = fmt == CONVROT_CODES_F16;
@@ -387,10 +483,12 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
   const int K_s = ((K + 15) / 16) * 16;
   const int f16 = fmt == CONVROT_CODES_F16;
   cudaError_t e;
+  // one 16-byte load per thread when every packed row starts 16-byte aligned
+  const bool w16 = (reinterpret_cast<uintptr_t>(w_fp4) % 16 == 0) && ((K_s / 2) % 16 == 0);
   switch (g.nbmax) {
-    case 1: e = launch_weight_nb<1>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
-    case 2: e = launch_weight_nb<2>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
-    default: e = launch_weight_nb<4>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
+    case 1: e = launch_weight_w<1>(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
+    case 2: e = launch_weight_w<2>(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
+    default: e = launch_weight_w<4>(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
   }
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("prepare_weight launch", e);
 }

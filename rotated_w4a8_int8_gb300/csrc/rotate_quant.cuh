@@ -188,6 +188,8 @@ __device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk
                                             const BlockCols& c) {
   const int col = blk * kBlock + 2 * lane8;
   if (f16_codes) {
+    // rint on the FP32 product itself (cvt.rni): a magic-number add would let
+    // the compiler fuse it with the preceding multiply, rounding once instead
     __half2* q = reinterpret_cast<__half2*>(static_cast<__half*>(q_row) + col);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
