@@ -41,9 +41,10 @@ METRIC = "ms/layer and effective INT8 TOPS at M=19989 (QKV, FFN-down); % of INT8
 # the pages' QKV layer time on an A40 at M=19989 (context, another machine)
 PAGES_QKV_MS = 25.08
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM traffic of one GEMM launch at the QKV shape, from the ncu capture summarised in
-# profiles/gemm_tcgen05_qkv.md, valid for the gemm.cu source with this SHA-256 prefix.
-GEMM_TRAFFIC = {"sha256_16": None, "bytes": None}
+# DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from the ncu capture
+# summarised in profiles/gemm_tcgen05_qkv.md; valid only for the gemm.cu source whose SHA-256
+# starts with this prefix (otherwise the bench line reports traffic as null).
+GEMM_TRAFFIC = {"sha256_16": "e0119d959c8dd011", "bytes": 2723842048 + 877882112}
 
 
 def sha16(path: str) -> str:
@@ -205,18 +206,6 @@ class Layer:
         self.act()
         self.gemm()
 
-    def e2e_step(self):
-        """Public API with host buffers: inputs in, layer, output out."""
-        import torch
-        if self.h_y is None:
-            self.h_y = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
-        self.x.copy_(self.h_x, non_blocking=True)
-        self.p.copy_(self.h_p, non_blocking=True)
-        self.s.copy_(self.h_s, non_blocking=True)
-        self.t.copy_(self.h_t, non_blocking=True)
-        self.step()
-        self.h_y.copy_(self.y, non_blocking=True)
-
 
 def time_layer(layer: Layer, steps: int, warmup: int, world: int, flush, sampler=None):
     """K timed steps; per-kernel CUDA events on the launching stream; L2 flushed
@@ -251,21 +240,85 @@ def time_layer(layer: Layer, steps: int, warmup: int, world: int, flush, sampler
     return dict(total_ms=sum(tot), step_ms=tot, weight_ms=w, act_ms=a, gemm_ms=g, clocks=clocks)
 
 
+class E2EPipeline:
+    """The layer through the public API with host buffers, pipelined over steps.
+
+    Every step copies its own inputs (x and the NVFP4 weight) from pinned host
+    memory, runs the three calls and copies its whole output back to pinned
+    host memory.  Three streams overlap step i+1's input copy and step i-1's
+    output copy with step i's kernels; device inputs and outputs are double
+    buffered and guarded by events.
+    """
+
+    def __init__(self, layer: Layer):
+        import torch
+        self.L = layer
+        self.torch = torch
+        dev = layer.x.device
+        self.s_in = torch.cuda.Stream(dev)
+        self.s_run = torch.cuda.Stream(dev)
+        self.s_out = torch.cuda.Stream(dev)
+        self.bufs = []
+        for _ in range(2):
+            self.bufs.append(dict(x=torch.empty_like(layer.x), p=torch.empty_like(layer.p),
+                                  s=torch.empty_like(layer.s), t=torch.empty_like(layer.t),
+                                  y=torch.empty_like(layer.y),
+                                  hy=torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory()))
+        self.in_bytes = layer.in_bytes
+        self.out_bytes = layer.y.numel() * layer.y.element_size()
+
+    def run(self, steps: int) -> float:
+        torch, L = self.torch, self.L
+        ev = lambda: torch.cuda.Event()
+        in_done = [None, None]       # inputs of the buffer landed
+        run_done = [None, None]      # kernels of the buffer finished (inputs free)
+        out_done = [None, None]      # output of the buffer copied out (y free)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(self.s_in)
+        for i in range(steps):
+            b = self.bufs[i % 2]
+            k = i % 2
+            with torch.cuda.stream(self.s_in):
+                if run_done[k] is not None:
+                    self.s_in.wait_event(run_done[k])
+                b["x"].copy_(L.h_x, non_blocking=True)
+                b["p"].copy_(L.h_p, non_blocking=True)
+                b["s"].copy_(L.h_s, non_blocking=True)
+                b["t"].copy_(L.h_t, non_blocking=True)
+                in_done[k] = ev()
+                in_done[k].record(self.s_in)
+            with torch.cuda.stream(self.s_run):
+                self.s_run.wait_event(in_done[k])
+                if out_done[k] is not None:
+                    self.s_run.wait_event(out_done[k])
+                L.cr.prepare_weight(b["p"], b["s"], b["t"], L.wl.K, L.wq, L.sw)
+                L.cr.quant_act(b["x"], L.wl.K, L.aq, L.sa, swiglu=L.wl.swiglu)
+                L.cr.gemm(L.aq, L.sa, L.wq, L.sw, b["y"])
+                run_done[k] = ev()
+                run_done[k].record(self.s_run)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(run_done[k])
+                b["hy"].copy_(b["y"], non_blocking=True)
+                out_done[k] = ev()
+                out_done[k].record(self.s_out)
+        self.s_out.wait_stream(self.s_in)
+        self.s_out.wait_stream(self.s_run)
+        t1.record(self.s_out)
+        t1.synchronize()
+        return t0.elapsed_time(t1)
+
+
 def time_e2e(layer: Layer, steps: int, warmup: int, world: int):
     import torch
-    for _ in range(warmup):
-        layer.e2e_step()
+    pipe = E2EPipeline(layer)
+    pipe.run(warmup)
     torch.cuda.synchronize()
     barrier(world)
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(steps):
-        layer.e2e_step()
-    e.record()
+    ms = pipe.run(steps)
     torch.cuda.synchronize()
     barrier(world)
-    return s.elapsed_time(e)
+    return ms, pipe.in_bytes, pipe.out_bytes
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
@@ -398,10 +451,12 @@ def main():
 
     # end-to-end through the public API with host buffers
     e2e_value = e2e_ms = None
-    if args.e2e_steps > 0:
-        e2e_ms = reduce_max(time_e2e(layer, args.e2e_steps, 3, world), world)
-        e2e_value = world * sz["ops"] * args.e2e_steps / (e2e_ms / 1e3) / 1e12
+    h2d = layer.in_bytes
     d2h = layer.y.numel() * layer.y.element_size()
+    if args.e2e_steps > 0:
+        e2e_ms, h2d, d2h = time_e2e(layer, args.e2e_steps, 3, world)
+        e2e_ms = reduce_max(e2e_ms, world)
+        e2e_value = world * sz["ops"] * args.e2e_steps / (e2e_ms / 1e3) / 1e12
     if layer.cr.device_error() != 0:
         raise SystemExit("device timeout reported by the GEMM")
 
@@ -463,8 +518,8 @@ def main():
                      "peak_source": f"{peaks_src} bf16_tflops_sustained (FP16 = BF16 rate)",
                      "work_per_launch": f"2*M*N*K_p = {sz['gemm_flops']:.4e} FLOP"},
         "hbm_peak_gbs": hbm,
-        "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": layer_in_bytes(wl),
-                "d2h_bytes_per_step": d2h,
+        "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "pipelined": "3 streams: copy-in, kernels, copy-out",
                 "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None},
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],
@@ -473,12 +528,6 @@ def main():
         "vs_baseline_note": "value / the pages' A40 QKV layer (25.08 ms = 184.3 TOPS): context only",
     }
     print(json.dumps(line), flush=True)
-
-
-def layer_in_bytes(wl):
-    esz = {"bf16": 2, "fp16": 2, "fp32": 4}[wl.x_dtype]
-    Ks = synth.stored_k(wl.K)
-    return wl.M * wl.k_in * esz + wl.N * Ks // 2 + wl.N * Ks // 16 + 4
 
 
 if __name__ == "__main__":
