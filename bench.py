@@ -403,6 +403,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--secondary", default="ffn_down",
                     help="second workload timed in the same run ('' to skip)")
+    ap.add_argument("--others", default="ffn_up,ragged,wide_k",
+                    help="further workloads timed briefly in the same run ('' to skip)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--rows", type=int, default=0,
                     help="truncate M to this many tokens (small profiling case; not a bench line)")
@@ -493,6 +495,21 @@ def main():
         del l2y
         torch.cuda.empty_cache()
 
+    others = {}
+    for name in [n for n in args.others.split(",") if n]:
+        wlo = synth.WORKLOADS[name]
+        lo = Layer(wlo, dev)
+        ro = time_layer(lo, 20, args.warmup, world, flush)
+        so = lo.sz
+        mso = reduce_max(ro["total_ms"], world) / len(ro["step_ms"])
+        others[name] = {"workload": f"M={wlo.M} K={wlo.K} N={wlo.N} {wlo.x_dtype}->{wlo.out_dtype}",
+                        "ms_per_layer": mso, "eff_tops": so["ops"] / (mso / 1e3) / 1e12,
+                        "gemm_tflops": so["gemm_flops"] / (statistics.mean(ro["gemm_ms"]) / 1e3) / 1e12,
+                        "quant_act_gbs": so["act_bytes"] / (statistics.mean(ro["act_ms"]) / 1e3) / 1e9,
+                        "prepare_weight_gbs": so["w_bytes"] / (statistics.mean(ro["weight_ms"]) / 1e3) / 1e9}
+        del lo
+        torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         cpu = cpu_baseline(wl, args.cpu_budget)
@@ -525,6 +542,7 @@ def main():
         "clocks": r["clocks"],
         "cpu_baseline": cpu,
         "secondary": secondary,
+        "others": others,
         "vs_baseline_note": "value / the pages' A40 QKV layer (25.08 ms = 184.3 TOPS): context only",
     }
     print(json.dumps(line), flush=True)
