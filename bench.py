@@ -145,13 +145,20 @@ def barrier(world):
 
 
 def reduce_max(v: float, world: int) -> float:
+    """Maximum of v over the ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tops(ops_per_step: float, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job throughput: every rank runs its own replica of the step."""
+    return world * ops_per_step * steps / (max_ms / 1e3) / 1e12
 
 
 # ---------------------------------------------------------------- GPU layer
@@ -441,7 +448,7 @@ def main():
     r = time_layer(layer, args.steps, args.warmup, world, flush, ClockSampler(bus))
     t_max = reduce_max(r["total_ms"], world)
     ms_step = t_max / args.steps
-    value = world * sz["ops"] * args.steps / (t_max / 1e3) / 1e12
+    value = aggregate_tops(sz["ops"], args.steps, t_max, world)
     g_ms = statistics.mean(r["gemm_ms"])
     a_ms = statistics.mean(r["act_ms"])
     w_ms = statistics.mean(r["weight_ms"])
@@ -458,7 +465,7 @@ def main():
     if args.e2e_steps > 0:
         e2e_ms, h2d, d2h = time_e2e(layer, args.e2e_steps, 3, world)
         e2e_ms = reduce_max(e2e_ms, world)
-        e2e_value = world * sz["ops"] * args.e2e_steps / (e2e_ms / 1e3) / 1e12
+        e2e_value = aggregate_tops(sz["ops"], args.e2e_steps, e2e_ms, world)
     if layer.cr.device_error() != 0:
         raise SystemExit("device timeout reported by the GEMM")
 

@@ -91,7 +91,8 @@ const char* convrot_status_string(int status);
  * s_w = fp32(max|r| / 127); q = clamp(rint(r * fp32(1/s_w)), -127, 127), the
  * product and rounding done in FP32 (half to even).  A row whose s_w is 0 or
  * whose reciprocal overflows is written as all-zero codes with s_w = 0.
- * Alignment: w_fp4 8-byte aligned; F16 codes: w_q 2-byte aligned.
+ * Alignment: w_fp4 8-byte aligned; w_q 4-byte (F16 codes) or 2-byte (S8
+ * codes) aligned with ld_wq even (codes are written in pairs).
  */
 int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
                            const float* w_tensor_scale, int N, int K,
@@ -113,8 +114,9 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
  *
  * Quantiser as for the weights (FP32 scale, FP32 reciprocal, FP32 product,
  * round half to even, clamp to +-127).  FP16 inputs are widened to FP32
- * before anything else.  x needs only element alignment; 16-byte aligned
- * rows take the vectorised load path.
+ * before anything else.  x needs only element alignment; rows aligned to 32
+ * or 16 bytes take the vectorised load paths.  a_q is 4-byte (F16 codes) or
+ * 2-byte (S8 codes) aligned with ld_aq even (codes are written in pairs).
  */
 int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
                       int M, int K, int swiglu,
@@ -136,7 +138,9 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
  * y[m, n] = fp32(acc) * s_a[m] * s_w[n] in FP32, rounded to out_dtype
  * (nearest even).  acc is the exact int32 sum over K_p.
  * Alignment: a_q and w_q 16-byte aligned with ld_aq, ld_wq multiples of 8
- * (TMA rule); out needs only element alignment.
+ * (TMA rule); out needs only element alignment (a 16-byte aligned out with a
+ * 16-byte multiple pitch is written by TMA tensor stores, any other by
+ * per-element stores).
  */
 int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale,
                  const void* w_q, int64_t ld_wq, const float* w_scale,

@@ -47,6 +47,8 @@ ACT_CASES = [
     ("swiglu_fp32_ragged", synth.Workload("sw32", 21, 300, 8, "fp32", "bf16", True, 0.0, 1.0, 11)),
     ("k16", synth.Workload("k16", 17, 16, 8, "bf16", "bf16", False, 0.0, 1.0, 12)),
     ("k1", synth.Workload("k1", 5, 1, 8, "bf16", "bf16", False, 0.0, 1.0, 13)),
+    ("max_kp", synth.Workload("maxkp", 3, 65536, 8, "bf16", "bf16", False, 0.01, 20.0, 17)),
+    ("max_kp_swiglu", synth.Workload("maxkps", 2, 65536, 8, "bf16", "bf16", True, 0.0, 1.0, 18)),
 ]
 
 
@@ -103,6 +105,7 @@ W_CASES = [
     ("ragged_rows", small("ragged", 8, 257)),
     ("wide_rows", small("wide_k", 8, 64)),
     ("k40", synth.Workload("k40", 8, 40, 24, "bf16", "bf16", False, 0.0, 1.0, 16)),
+    ("max_kp", synth.Workload("maxkpw", 8, 65536, 5, "bf16", "bf16", False, 0.0, 1.0, 19)),
 ]
 
 
@@ -131,7 +134,7 @@ def test_prepare_weight_ignores_serialised_padding():
 
 # ---------------------------------------------------------------- kernel 3
 GEMM_SHAPES = [(128, 256, 256), (300, 520, 1280), (1, 1, 256), (129, 257, 768), (513, 300, 5376),
-               (64, 1000, 512)]
+               (64, 1000, 512), (130, 260, 65536)]
 
 
 @pytest.mark.parametrize("M,N,Kp", GEMM_SHAPES)
