@@ -615,7 +615,14 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int
 template <int OUT>
 static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                           const Params& p, cudaStream_t st) {
-  static int max_clusters = 0;   // per process and instantiation; one device per process
+  static int max_clusters_by_dev[64] = {0};   // resident clusters, per device and instantiation
+  int dev = 0;
+  {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+  }
+  int dummy = 0;
+  int& max_clusters = (dev >= 0 && dev < 64) ? max_clusters_by_dev[dev] : dummy;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -631,8 +638,7 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CU
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     cfg.gridDim = dim3(sms / CLUSTER * CLUSTER);
     int n = 0;
