@@ -100,15 +100,19 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
                            float* w_scale, cudaStream_t stream);
 
 /*
- * Activation quantisation: optional SwiGLU prologue, then ConvRot256 rotation
- * in FP32 and row-scaled S8 quantisation (the page's "Pre-scales and SwiGLU
- * run before rotation" and "SwiGLU is fused with rotation/A8 quantization").
+ * Activation quantisation: optional SwiGLU prologue, optional channel
+ * pre-scales, then ConvRot256 rotation in FP32 and row-scaled S8 quantisation
+ * (the page's "Pre-scales and SwiGLU run before rotation" and "SwiGLU is
+ * fused with rotation/A8 quantization").
  *
  *   x       [M][ld_x] in x_dtype (BF16 / FP16 / FP32).  swiglu == 0: columns
  *           0..K-1 are the input.  swiglu != 0: columns 0..K-1 are the gate
  *           g and K..2K-1 the value v, and the layer input is
  *           h = g * sigmoid(g) * v computed in FP32 with no intermediate
  *           rounding.  ld_x >= K (or 2K).
+ *   pre_scale  NULL, or [K] FP32 channel multipliers (16-byte aligned): the
+ *           layer input becomes h[m, k] * pre_scale[k] (after SwiGLU, before
+ *           the rotation, in FP32).
  *   a_q     [M][ld_aq] codes in `fmt`, columns 0..K_p-1 written; ld_aq >= K_p.
  *   a_scale [M] FP32 token scales s_a (0 for a degenerate row).
  *
@@ -119,7 +123,7 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
  * 2-byte (S8 codes) aligned with ld_aq even (codes are written in pairs).
  */
 int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
-                      int M, int K, int swiglu,
+                      int M, int K, int swiglu, const float* pre_scale,
                       void* a_q, convrot_codes fmt, int64_t ld_aq,
                       float* a_scale, cudaStream_t stream);
 
@@ -130,13 +134,14 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
  *
  *   a_q     [M][ld_aq] FP16-stored S8 codes of the rotated activations.
  *   w_q     [N][ld_wq] FP16-stored S8 codes of the rotated weights.
- *   a_scale [M], w_scale [N] FP32 row scales.
+ *   a_scale [M], w_scale [N] FP32 row scales (w_scale 16-byte aligned).
+ *   bias    NULL, or [N] FP32 per-output-channel bias (16-byte aligned).
  *   K_p     padded reduction width, a multiple of 256, <= CONVROT_MAX_KP.
  *   out     [M][ld_out] in out_dtype; ld_out >= N.  Only columns 0..N-1 of
  *           rows 0..M-1 are written.
  *
- * y[m, n] = fp32(acc) * s_a[m] * s_w[n] in FP32, rounded to out_dtype
- * (nearest even).  acc is the exact int32 sum over K_p.
+ * y[m, n] = fp32(acc) * s_a[m] * s_w[n] (+ bias[n]) in FP32, rounded to
+ * out_dtype (nearest even).  acc is the exact int32 sum over K_p.
  * Alignment: a_q and w_q 16-byte aligned with ld_aq, ld_wq multiples of 8
  * (TMA rule); out needs only element alignment (a 16-byte aligned out with a
  * 16-byte multiple pitch is written by TMA tensor stores, any other by
@@ -144,7 +149,7 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
  */
 int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale,
                  const void* w_q, int64_t ld_wq, const float* w_scale,
-                 int M, int N, int K_p,
+                 const float* bias, int M, int N, int K_p,
                  void* out, convrot_dtype out_dtype, int64_t ld_out,
                  cudaStream_t stream);
 

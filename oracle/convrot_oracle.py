@@ -239,11 +239,19 @@ def round_to_dtype(y: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
-def dequantize(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray, out_dtype: str) -> np.ndarray:
-    """y[m, n] = acc[m, n] * s_a[m] * s_w[n] in FP64, then one rounding to out_dtype."""
+def dequantize(acc: np.ndarray, sa: np.ndarray, sw: np.ndarray, out_dtype: str,
+               bias: np.ndarray | None = None) -> np.ndarray:
+    """y[m, n] = acc[m, n] * s_a[m] * s_w[n] (+ bias[n]) in FP64, then one rounding.
+
+    The bias is the linear layer's y = x W^T + b (MiniMax-H3 explainer on
+    modelpad.app, "Foundations"); the ConvRot entry names none, so it is
+    optional.
+    """
     y = (np.asarray(acc, dtype=np.float64)
          * np.asarray(sa, dtype=np.float64)[:, None]
          * np.asarray(sw, dtype=np.float64)[None, :])
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float32).astype(np.float64)[None, :]
     return round_to_dtype(y, out_dtype)
 
 
@@ -268,18 +276,27 @@ def prepare_weight(packed, scales, tensor_scale, K: int):
     return quantize_rows(rotate_blocks(w))
 
 
-def quant_act(x_storage, x_dtype: str, K: int, swiglu_flag: bool = False):
-    """(SwiGLU ->) pad -> rotate -> row-scaled S8.  Returns (q_a, s_a)."""
+def quant_act(x_storage, x_dtype: str, K: int, swiglu_flag: bool = False, pre_scale=None):
+    """(SwiGLU ->) (channel pre-scale ->) pad -> rotate -> row-scaled S8.
+
+    Channel pre-scales multiply the layer's input h[:, k] by p[k] before the
+    rotation ("Pre-scales and SwiGLU run before rotation"; "Channel pre-scales
+    retain the correct unfused ordering": the scale belongs to this layer's
+    input, so it follows the SwiGLU that produces that input).
+    Returns (q_a, s_a).
+    """
     x = storage_to_f64(x_storage, x_dtype)
     h = swiglu(x, K) if swiglu_flag else x[:, :K]
+    if pre_scale is not None:
+        h = h * np.asarray(pre_scale, dtype=np.float32).astype(np.float64)[None, :K]
     return quantize_rows(rotate_blocks(h))
 
 
 def convrot_linear(x_storage, x_dtype, packed, scales, tensor_scale, K, out_dtype,
-                   swiglu_flag=False):
+                   swiglu_flag=False, pre_scale=None, bias=None):
     """The whole layer; returns (y as FP64 holding out_dtype values, intermediates)."""
     qw, sw = prepare_weight(packed, scales, tensor_scale, K)
-    qa, sa = quant_act(x_storage, x_dtype, K, swiglu_flag)
+    qa, sa = quant_act(x_storage, x_dtype, K, swiglu_flag, pre_scale)
     acc = int_gemm(qa, qw)
-    y = dequantize(acc, sa, sw, out_dtype)
+    y = dequantize(acc, sa, sw, out_dtype, bias)
     return y, dict(qa=qa, sa=sa, qw=qw, sw=sw, acc=acc)

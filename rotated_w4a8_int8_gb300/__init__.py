@@ -51,9 +51,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.convrot_status_string.restype = ctypes.c_char_p
     lib.convrot_prepare_weight.argtypes = [vp, vp, vp, i32, i32, vp, i32, i64, vp, vp]
     lib.convrot_prepare_weight.restype = i32
-    lib.convrot_quant_act.argtypes = [vp, i32, i64, i32, i32, i32, vp, i32, i64, vp, vp]
+    lib.convrot_quant_act.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, i32, i64, vp, vp]
     lib.convrot_quant_act.restype = i32
-    lib.convrot_gemm.argtypes = [vp, i64, vp, vp, i64, vp, i32, i32, i32, vp, i32, i64, vp]
+    lib.convrot_gemm.argtypes = [vp, i64, vp, vp, i64, vp, vp, i32, i32, i32, vp, i32, i64, vp]
     lib.convrot_gemm.restype = i32
     lib.convrot_gemm_i32.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp, i64, vp]
     lib.convrot_gemm_i32.restype = i32
@@ -116,23 +116,23 @@ def prepare_weight(w_fp4, w_sf, w_tensor_scale, K: int, w_q, w_scale, stream=Non
         w_q.stride(0), _ptr(w_scale), _stream(stream)))
 
 
-def quant_act(x, K: int, a_q, a_scale, swiglu: bool = False, stream=None) -> None:
+def quant_act(x, K: int, a_q, a_scale, swiglu: bool = False, pre_scale=None, stream=None) -> None:
     """convrot_quant_act: x bf16/fp16/fp32 [M, >=K or 2K], a_q int8 or float16
-    [M, >=K_p], a_scale float32 [M]."""
+    [M, >=K_p], a_scale float32 [M], pre_scale None or float32 [K]."""
     M = x.shape[0]
     _check("convrot_quant_act", load_library().convrot_quant_act(
-        _ptr(x), _dtype_code(x), x.stride(0), M, int(K), int(bool(swiglu)), _ptr(a_q),
-        _codes_fmt(a_q), a_q.stride(0), _ptr(a_scale), _stream(stream)))
+        _ptr(x), _dtype_code(x), x.stride(0), M, int(K), int(bool(swiglu)), _ptr(pre_scale),
+        _ptr(a_q), _codes_fmt(a_q), a_q.stride(0), _ptr(a_scale), _stream(stream)))
 
 
-def gemm(a_q, a_scale, w_q, w_scale, out, K_p: int | None = None, stream=None) -> None:
+def gemm(a_q, a_scale, w_q, w_scale, out, K_p: int | None = None, bias=None, stream=None) -> None:
     """convrot_gemm: a_q float16 codes [M, >=K_p], w_q float16 codes [N, >=K_p],
-    out bf16/fp16/fp32 [M, >=N] (N = w_q rows)."""
+    out bf16/fp16/fp32 [M, >=N] (N = w_q rows), bias None or float32 [N]."""
     M, N = a_q.shape[0], w_q.shape[0]
     K_p = a_q.shape[1] if K_p is None else K_p
     _check("convrot_gemm", load_library().convrot_gemm(
         _ptr(a_q), a_q.stride(0), _ptr(a_scale), _ptr(w_q), w_q.stride(0), _ptr(w_scale),
-        M, N, int(K_p), _ptr(out), _dtype_code(out), out.stride(0), _stream(stream)))
+        _ptr(bias), M, N, int(K_p), _ptr(out), _dtype_code(out), out.stride(0), _stream(stream)))
 
 
 def gemm_i32(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:

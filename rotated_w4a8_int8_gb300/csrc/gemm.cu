@@ -246,6 +246,7 @@ struct Params {
   int num_mp, num_pair_tiles;     // M-tile pairs (one per cluster) and pair tiles
   const float* a_scale;
   const float* w_scale;
+  const float* bias;   // optional, [N]
   void* out;
   int64_t ld_out;
   int out_vec;      // 16-byte vector stores allowed (base and pitch aligned)
@@ -488,21 +489,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             for (int c = 0; c < OUT_BOX_BYTES / 16; ++c) {
               const int j0 = b * CPB + c * VEC;            // first column of this chunk
               const int n = n0 + j0;
-              float sw[VEC];
+              float sw[VEC], bs[VEC];
               if (n + VEC <= p.N) {
 #pragma unroll
                 for (int q = 0; q < VEC; q += 4) {
                   const float4 f = __ldg(reinterpret_cast<const float4*>(p.w_scale + n + q));
                   sw[q] = f.x; sw[q + 1] = f.y; sw[q + 2] = f.z; sw[q + 3] = f.w;
+                  const float4 g = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + n + q))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                  bs[q] = g.x; bs[q + 1] = g.y; bs[q + 2] = g.z; bs[q + 3] = g.w;
                 }
               } else {
 #pragma unroll
-                for (int q = 0; q < VEC; ++q) sw[q] = (n + q < p.N) ? __ldg(p.w_scale + n + q) : 0.f;
+                for (int q = 0; q < VEC; ++q) {
+                  sw[q] = (n + q < p.N) ? __ldg(p.w_scale + n + q) : 0.f;
+                  bs[q] = (p.bias && n + q < p.N) ? __ldg(p.bias + n + q) : 0.f;
+                }
               }
               union { T v[VEC]; uint4 u; } pk;
 #pragma unroll
               for (int q = 0; q < VEC; ++q)
-                pk.v[q] = to_out<OUT>(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + q]), sa), sw[q]));
+                pk.v[q] = to_out<OUT>(__fadd_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + q]), sa), sw[q]), bs[q]));
               // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
               *reinterpret_cast<uint4*>(rowp + ((c ^ ((lane >> 1) & 3)) << 4)) = pk.u;
             }
@@ -523,8 +530,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
               union { T v[VEC]; uint4 u; } pk;
 #pragma unroll
               for (int j = 0; j < VEC; ++j) {
-                const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa),
-                                          __ldg(p.w_scale + n + j));
+                const float y = __fadd_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa),
+                                                    __ldg(p.w_scale + n + j)),
+                                          p.bias ? __ldg(p.bias + n + j) : 0.f);
                 pk.v[j] = to_out<OUT>(y);
               }
               *reinterpret_cast<uint4*>(orow + n) = pk.u;
@@ -532,8 +540,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 #pragma unroll
               for (int j = 0; j < VEC; ++j) {
                 if (n + j < p.N) {
-                  const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa),
-                                            __ldg(p.w_scale + n + j));
+                  const float y = __fadd_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa),
+                                                      __ldg(p.w_scale + n + j)),
+                                            p.bias ? __ldg(p.bias + n + j) : 0.f);
                   orow[n + j] = to_out<OUT>(y);
                 }
               }
@@ -668,10 +677,11 @@ static int validate_operands(const void* a_q, int64_t ld_aq, const void* w_q, in
 }
 
 static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scale, const void* w_q,
-               int64_t ld_wq, const float* w_scale, int M, int N, int K_p, void* out, int64_t ld_out,
-               size_t out_esize, cudaStream_t stream, int test_stall = 0) {
+               int64_t ld_wq, const float* w_scale, const float* bias, int M, int N, int K_p, void* out,
+               int64_t ld_out, size_t out_esize, cudaStream_t stream, int test_stall = 0) {
   Params p;
   p.test_stall = test_stall;
+  p.bias = bias;
   p.M = M;
   p.N = N;
   p.K_p = K_p;
@@ -707,8 +717,8 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
 using namespace crgemm;
 
 extern "C" int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale, const void* w_q,
-                            int64_t ld_wq, const float* w_scale, int M, int N, int K_p, void* out,
-                            convrot_dtype out_dtype, int64_t ld_out, cudaStream_t stream) {
+                            int64_t ld_wq, const float* w_scale, const float* bias, int M, int N, int K_p,
+                            void* out, convrot_dtype out_dtype, int64_t ld_out, cudaStream_t stream) {
   if (out_dtype != CONVROT_BF16 && out_dtype != CONVROT_FP16 && out_dtype != CONVROT_FP32)
     return CONVROT_ERR_UNSUPPORTED;
   int st = validate_operands(a_q, ld_aq, w_q, ld_wq, M, N, K_p);
@@ -717,10 +727,11 @@ extern "C" int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale
   if (M == 0 || N == 0) return CONVROT_OK;
   if (!a_scale || !w_scale || !out) return CONVROT_ERR_INVALID_ARG;
   const size_t es = out_dtype == CONVROT_FP32 ? 4 : 2;
+  // w_scale and bias are read four at a time: 16-byte aligned
   if (reinterpret_cast<uintptr_t>(out) % es || reinterpret_cast<uintptr_t>(a_scale) % 4 ||
-      reinterpret_cast<uintptr_t>(w_scale) % 4)
+      reinterpret_cast<uintptr_t>(w_scale) % 16 || reinterpret_cast<uintptr_t>(bias) % 16)
     return CONVROT_ERR_MISALIGNED;
-  return run(out_dtype, a_q, ld_aq, a_scale, w_q, ld_wq, w_scale, M, N, K_p, out, ld_out, es, stream);
+  return run(out_dtype, a_q, ld_aq, a_scale, w_q, ld_wq, w_scale, bias, M, N, K_p, out, ld_out, es, stream);
 }
 
 extern "C" int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const void* w_q, int64_t ld_wq, int M,
@@ -731,7 +742,7 @@ extern "C" int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const void* w_q,
   if (M == 0 || N == 0) return CONVROT_OK;
   if (!acc) return CONVROT_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(acc) % 4) return CONVROT_ERR_MISALIGNED;
-  return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, M, N, K_p, acc, ld_acc, 4, stream);
+  return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, nullptr, M, N, K_p, acc, ld_acc, 4, stream);
 }
 
 extern "C" int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, const void* w_q,
@@ -741,7 +752,7 @@ extern "C" int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, con
   if (st != CONVROT_OK) return st;
   if (M == 0 || N == 0 || !acc || ld_acc < N) return CONVROT_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(acc) % 4) return CONVROT_ERR_MISALIGNED;
-  return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, M, N, K_p, acc, ld_acc, 4, stream, 1);
+  return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, nullptr, M, N, K_p, acc, ld_acc, 4, stream, 1);
 }
 
 extern "C" int convrot_device_error(cudaStream_t stream, int* code) {

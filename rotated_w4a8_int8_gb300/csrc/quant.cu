@@ -191,12 +191,32 @@ __device__ __forceinline__ void load_act_row(const char* xrow, int K, int nblock
   }
 }
 
-// One activation row from its raw input: (SwiGLU,) rotation, CTA absmax,
-// scale and codes.  `red` is this row's reduction buffer.
+// Channel pre-scales p[c0 .. c0+31] applied to the pass-1 pairs
+// P[b] = (elem b, elem 16 + b); nothing at or past K is read.
+__device__ __forceinline__ void apply_pre_scale(const float* __restrict__ p, int c0, int K, float2 (&P)[16]) {
+  if (c0 >= K) return;
+  float ps[32];
+  if (c0 + 32 <= K) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(p + c0) + u);
+      ps[4 * u] = f.x; ps[4 * u + 1] = f.y; ps[4 * u + 2] = f.z; ps[4 * u + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) ps[e] = (c0 + e < K) ? __ldg(p + c0 + e) : 0.f;
+  }
+#pragma unroll
+  for (int b = 0; b < 16; ++b) P[b] = mul2(P[b], make_float2(ps[b], ps[16 + b]));
+}
+
+// One activation row from its raw input: (SwiGLU,) (channel pre-scale,)
+// rotation, CTA absmax, scale and codes.  `red` is this row's reduction buffer.
 template <int DT, bool SWIGLU, int NBMAX>
-__device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, int row, int nblocks, int S,
-                                        int slot, int lane8, char* my, float* red, void* q, int f16_codes,
-                                        int64_t ld_q, float* scale) {
+__device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, int row, int K, int nblocks,
+                                        int S, int slot, int lane8, char* my, float* red,
+                                        const float* pre_scale, void* q, int f16_codes, int64_t ld_q,
+                                        float* scale) {
   BlockCols c[NBMAX];
   float amax = 0.f;
 #pragma unroll
@@ -207,6 +227,7 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
     if (active) {
       if constexpr (SWIGLU) pairs_swiglu<DT>(cur.g[i], cur.v[SWIGLU ? i : 0], P);
       else pairs_from_raw<DT>(cur.g[i], P);
+      if (pre_scale) apply_pre_scale(pre_scale, blk * kBlock + 32 * lane8, K, P);
     }
     rotate_block(P, c[i], my, lane8, active);
     if (active) amax = absmax_cols(amax, c[i]);
@@ -230,7 +251,8 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
 template <int DT, bool SWIGLU, int NBMAX, int VEC>
 __global__ void __launch_bounds__(kMaxThreads)
 quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S,
-                 void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
+                 const float* __restrict__ pre_scale, void* __restrict__ q, int f16_codes, int64_t ld_q,
+                 float* __restrict__ scale) {
   extern __shared__ __align__(16) char smem[];
   float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);   // per-warp maxima
   const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
@@ -239,8 +261,8 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nbl
   ActRaw<DT, SWIGLU, NBMAX> cur;
   load_act_row<DT, SWIGLU, NBMAX, VEC>(static_cast<const char*>(x) + static_cast<size_t>(row) * ld_x * esize,
                                        K, nblocks, S, slot, lane8, cur);
-  act_row<DT, SWIGLU, NBMAX>(cur, row, nblocks, S, slot, lane8, smem + slot * kSlotBytes, red, q, f16_codes,
-                             ld_q, scale);
+  act_row<DT, SWIGLU, NBMAX>(cur, row, K, nblocks, S, slot, lane8, smem + slot * kSlotBytes, red, pre_scale, q,
+                             f16_codes, ld_q, scale);
 }
 
 // Raw NVFP4 input of one weight row for this thread.
@@ -367,39 +389,39 @@ static cudaError_t prep_smem(Kern k, size_t smem) {
 
 template <int DT, bool SWIGLU, int VEC, int NB>
 static cudaError_t launch_act_nb(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
-                                 void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
+                                 const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
   auto k = quant_act_kernel<DT, SWIGLU, NB, VEC>;
   cudaError_t e = prep_smem(k, g.smem);
   if (e != cudaSuccess) return e;
-  k<<<M, g.threads, g.smem, st>>>(x, ld_x, M, K, g.nblocks, g.S, q, f16, ld_q, scale);
+  k<<<M, g.threads, g.smem, st>>>(x, ld_x, M, K, g.nblocks, g.S, ps, q, f16, ld_q, scale);
   return cudaGetLastError();
 }
 
 template <int DT, bool SWIGLU, int VEC>
 static cudaError_t launch_act_dt(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
-                                 void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
+                                 const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
   switch (g.nbmax) {
-    case 1: return launch_act_nb<DT, SWIGLU, VEC, 1>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
-    case 2: return launch_act_nb<DT, SWIGLU, VEC, 2>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
-    default: return launch_act_nb<DT, SWIGLU, VEC, 4>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    case 1: return launch_act_nb<DT, SWIGLU, VEC, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+    case 2: return launch_act_nb<DT, SWIGLU, VEC, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+    default: return launch_act_nb<DT, SWIGLU, VEC, 4>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
   }
 }
 
 template <int DT>
 static cudaError_t launch_act(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
-                              bool swiglu, int vec, void* q, int f16, int64_t ld_q, float* scale,
-                              cudaStream_t st) {
+                              bool swiglu, int vec, const float* ps, void* q, int f16, int64_t ld_q,
+                              float* scale, cudaStream_t st) {
   if (swiglu) {
     switch (vec) {
-      case 2: return launch_act_dt<DT, true, 2>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
-      case 1: return launch_act_dt<DT, true, 1>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
-      default: return launch_act_dt<DT, true, 0>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+      case 2: return launch_act_dt<DT, true, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+      case 1: return launch_act_dt<DT, true, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+      default: return launch_act_dt<DT, true, 0>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
     }
   }
   switch (vec) {
-    case 2: return launch_act_dt<DT, false, 2>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
-    case 1: return launch_act_dt<DT, false, 1>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
-    default: return launch_act_dt<DT, false, 0>(g, M, x, ld_x, K, q, f16, ld_q, scale, st);
+    case 2: return launch_act_dt<DT, false, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+    case 1: return launch_act_dt<DT, false, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+    default: return launch_act_dt<DT, false, 0>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
   }
 }
 
@@ -427,8 +449,8 @@ static cudaError_t launch_weight_w(const RowGeometry& g, bool w16, int N, const 
 using namespace convrot;
 
 extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x, int M, int K,
-                                 int swiglu, void* a_q, convrot_codes fmt, int64_t ld_aq,
-                                 float* a_scale, cudaStream_t stream) {
+                                 int swiglu, const float* pre_scale, void* a_q, convrot_codes fmt,
+                                 int64_t ld_aq, float* a_scale, cudaStream_t stream) {
   if (M < 0 || K <= 0) return CONVROT_ERR_INVALID_ARG;
   if (x_dtype != CONVROT_BF16 && x_dtype != CONVROT_FP16 && x_dtype != CONVROT_FP32)
     return CONVROT_ERR_UNSUPPORTED;
@@ -443,7 +465,8 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
   if (reinterpret_cast<uintptr_t>(x) % esize) return CONVROT_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(a_q) % (fmt == CONVROT_CODES_F16 ? 4 : 2) || ld_aq % 2)
     return CONVROT_ERR_MISALIGNED;
-  if (reinterpret_cast<uintptr_t>(a_scale) % 4) return CONVROT_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(a_scale) % 4 || reinterpret_cast<uintptr_t>(pre_scale) % 16)
+    return CONVROT_ERR_MISALIGNED;
   // vector paths: every row start and the value half (SwiGLU) aligned to 32 or 16 bytes
   auto aligned = [&](int64_t a) {
     return (reinterpret_cast<uintptr_t>(x) % a == 0) && ((ld_x * static_cast<int64_t>(esize)) % a == 0) &&
@@ -455,9 +478,9 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
   const int f16 = fmt == CONVROT_CODES_F16;
   cudaError_t e;
   switch (x_dtype) {
-    case CONVROT_BF16: e = launch_act<DT_BF16>(g, M, x, ld_x, K, swiglu != 0, vec, a_q, f16, ld_aq, a_scale, stream); break;
-    case CONVROT_FP16: e = launch_act<DT_FP16>(g, M, x, ld_x, K, swiglu != 0, vec, a_q, f16, ld_aq, a_scale, stream); break;
-    default: e = launch_act<DT_FP32>(g, M, x, ld_x, K, swiglu != 0, vec, a_q, f16, ld_aq, a_scale, stream); break;
+    case CONVROT_BF16: e = launch_act<DT_BF16>(g, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, stream); break;
+    case CONVROT_FP16: e = launch_act<DT_FP16>(g, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, stream); break;
+    default: e = launch_act<DT_FP32>(g, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, stream); break;
   }
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("quant_act launch", e);
 }

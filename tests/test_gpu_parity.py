@@ -209,8 +209,8 @@ def test_empty_calls_launch_nothing():
     import rotated_w4a8_int8_gb300 as cr
     lib = cr.load_library()
     y = torch.full((4, 4), 3.0, device=DEV)
-    assert lib.convrot_gemm(16, 512, 16, 16, 512, 16, 0, 4, 512, y.data_ptr(), 2, 4, 0) == 0
-    assert lib.convrot_quant_act(16, 0, 512, 0, 512, 0, 16, 1, 512, 16, 0) == 0
+    assert lib.convrot_gemm(16, 512, 16, 16, 512, 16, None, 0, 4, 512, y.data_ptr(), 2, 4, 0) == 0
+    assert lib.convrot_quant_act(16, 0, 512, 0, 512, 0, None, 16, 1, 512, 16, 0) == 0
     torch.cuda.synchronize()
     assert torch.all(y == 3.0)
 
@@ -243,4 +243,35 @@ def test_layer_matches_oracle(case, wl):
     Kp = oracle.padded_k(wl.K)
     assert_codes_match(codes_to_np(qa, Kp), mid["qa"])
     assert_codes_match(codes_to_np(qw, Kp), mid["qw"])
+    assert_output_match(y.float().cpu().numpy(), ref)
+
+
+PS_CASES = [
+    ("bf16_swiglu", synth.Workload("ps1", 70, 1000, 300, "bf16", "bf16", True, 0.0, 1.0, 23)),
+    ("fp16_plain", synth.Workload("ps2", 130, 768, 520, "fp16", "fp32", False, 0.02, 20.0, 24)),
+    ("fp32_in", synth.Workload("ps3", 33, 512, 257, "fp32", "fp16", False, 0.0, 1.0, 25)),
+]
+
+
+@pytest.mark.parametrize("case,wl", PS_CASES, ids=[c[0] for c in PS_CASES])
+def test_layer_with_channel_pre_scale_and_bias(case, wl):
+    rng = np.random.default_rng(wl.seed)
+    pre = np.exp(rng.uniform(-1.5, 1.5, wl.K)).astype(np.float32)
+    bias = (rng.standard_normal(wl.N) * 0.5).astype(np.float32)
+    x = synth.make_activations(wl)
+    packed, scales, t = synth.make_nvfp4_weight(wl)
+    Kp = oracle.padded_k(wl.K)
+    qw, sw = gpu_prepare_weight(packed, scales, t, wl.K)
+    xd = storage_to_dev(x, wl.x_dtype)
+    qa = torch.empty(wl.M, Kp, dtype=torch.float16, device=DEV)
+    sa = torch.empty(wl.M, dtype=torch.float32, device=DEV)
+    import rotated_w4a8_int8_gb300 as cr
+    cr.quant_act(xd, wl.K, qa, sa, swiglu=wl.swiglu, pre_scale=torch.from_numpy(pre).to(DEV))
+    from gpu_util import TORCH_DT
+    y = torch.empty(wl.M, wl.N, dtype=TORCH_DT[wl.out_dtype], device=DEV)
+    cr.gemm(qa, sa, qw, sw, y, bias=torch.from_numpy(bias).to(DEV))
+    ref, mid = oracle.convrot_linear(x, wl.x_dtype, packed, scales, t, wl.K, wl.out_dtype, wl.swiglu,
+                                     pre_scale=pre, bias=bias)
+    assert_codes_match(codes_to_np(qa, Kp), mid["qa"])
+    assert_scales_match(sa.cpu().numpy(), mid["sa"])
     assert_output_match(y.float().cpu().numpy(), ref)

@@ -321,3 +321,40 @@ def test_synth_shapes_follow_the_pages():
     assert W["qkv"].K == g["hidden"] and W["qkv"].N == g["qkv_out"]
     assert W["ffn_down"].K == g["ffn_hidden"] and W["ffn_down"].k_in == g["fc1_out"]
     assert W["ffn_up"].N == g["fc1_out"]
+
+
+# ---------------------------------------------------------------- pre-scales and bias
+def test_pre_scale_folds_into_the_weights():
+    # (x * p) W'^T with W' = W / p equals x W^T: the pre-scale acts on the
+    # layer input before the rotation, and the rotation stays paired
+    rng = np.random.default_rng(41)
+    K = 512
+    x = rng.standard_normal((6, K))
+    w = rng.standard_normal((5, K))
+    p = np.exp(rng.uniform(-2, 2, K))
+    xs = x * p
+    ws = w / p
+    lhs = oracle.rotate_blocks(xs) @ oracle.rotate_blocks(ws).T
+    assert np.allclose(lhs, x @ w.T, rtol=1e-10, atol=1e-10)
+
+
+def test_pre_scale_applies_after_swiglu_and_before_rotation():
+    K = 256
+    x2 = np.zeros((1, 2 * K), np.float32)
+    x2[0, 3] = 1.0            # gate 1 at channel 3
+    x2[0, K + 3] = 2.0        # value 2 at channel 3
+    p = np.ones(K, np.float32)
+    p[3] = 4.0
+    bits = synth.bf16_bits_from_f32(x2)
+    q, s = oracle.quant_act(bits, "bf16", K, True, p)
+    h3 = 1.0 / (1.0 + math.exp(-1.0)) * 2.0 * 4.0     # swish(1) * 2, then * 4
+    # a single nonzero channel rotates to +-h3/16 everywhere: codes +-127
+    assert np.all(np.abs(q) == 127)
+    assert abs(float(s[0]) - np.float32(np.float32(h3 / 16) / np.float32(127))) <= 2e-7 * h3
+
+
+def test_bias_adds_per_output_channel():
+    acc = np.zeros((2, 3), np.int64)
+    b = np.array([0.5, -1.0, 2.0], np.float32)
+    y = oracle.dequantize(acc, np.ones(2, np.float32), np.ones(3, np.float32), "fp32", b)
+    assert np.array_equal(y, np.array([[0.5, -1.0, 2.0], [0.5, -1.0, 2.0]]))
