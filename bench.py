@@ -340,6 +340,66 @@ def time_e2e(layer: Layer, steps: int, warmup: int, world: int):
     return ms, pipe.in_bytes, pipe.out_bytes
 
 
+def time_ffn_block(dev, world, flush, warmup, steps=10):
+    """The MiniMax-H3 FFN block at M = 19989: fc1 (28672 x 5376) with its NVFP4
+    weight prepared, the fused SwiGLU + rotation + S8 of its BF16 output, and
+    fc2 (5376 x 14336) with its weight prepared: six kernel launches per step."""
+    import torch
+
+    import rotated_w4a8_int8_gb300 as cr
+    up = synth.WORKLOADS["ffn_up"]
+    up = dataclasses.replace(up, x_dtype="bf16", out_dtype="bf16")
+    down = synth.WORKLOADS["ffn_down"]
+    M, H, F = up.M, up.K, down.K
+    x = synth.make_activations(up)
+    p1, s1, t1 = synth.make_nvfp4_weight(up)
+    p2, s2, t2 = synth.make_nvfp4_weight(down)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    P1, S1, T1 = (torch.from_numpy(p1).to(dev), torch.from_numpy(s1).to(dev),
+                  torch.tensor([float(t1)], dtype=torch.float32, device=dev))
+    P2, S2, T2 = (torch.from_numpy(p2).to(dev), torch.from_numpy(s2).to(dev),
+                  torch.tensor([float(t2)], dtype=torch.float32, device=dev))
+    Hp, Fp = cr.padded_k(H), cr.padded_k(F)
+    w1 = torch.empty(2 * F, Hp, dtype=torch.float16, device=dev)
+    sw1 = torch.empty(2 * F, dtype=torch.float32, device=dev)
+    w2 = torch.empty(H, Fp, dtype=torch.float16, device=dev)
+    sw2 = torch.empty(H, dtype=torch.float32, device=dev)
+    xq = torch.empty(M, Hp, dtype=torch.float16, device=dev)
+    sx = torch.empty(M, dtype=torch.float32, device=dev)
+    h2 = torch.empty(M, 2 * F, dtype=torch.bfloat16, device=dev)
+    hq = torch.empty(M, Fp, dtype=torch.float16, device=dev)
+    sh = torch.empty(M, dtype=torch.float32, device=dev)
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+
+    def step():
+        cr.prepare_weight(P1, S1, T1, H, w1, sw1)
+        cr.quant_act(xd, H, xq, sx)
+        cr.gemm(xq, sx, w1, sw1, h2)
+        cr.prepare_weight(P2, S2, T2, F, w2, sw2)
+        cr.quant_act(h2, F, hq, sh, swiglu=True)
+        cr.gemm(hq, sh, w2, sw2, y)
+
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    tot = 0.0
+    for _ in range(steps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    ms = reduce_max(tot, world) / steps
+    ops = 2.0 * M * (2 * F) * H + 2.0 * M * H * F
+    return {"workload": f"FFN block M={M}: fc1 {2 * F}x{H} -> SwiGLU -> fc2 {H}x{F}, BF16",
+            "ms_per_block": ms, "eff_tops": ops / (ms / 1e3) / 1e12, "kernels_per_step": 6}
+
+
 # ---------------------------------------------------------------- CPU oracle baseline
 class OracleSample:
     """The first m tokens x first n weight rows of a workload, generated once;
@@ -425,6 +485,8 @@ def main():
     ap.add_argument("--others", default="ffn_up,ragged,wide_k",
                     help="further workloads timed briefly in the same run ('' to skip)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ffn-block", type=int, default=1,
+                    help="also time the FFN block fc1 -> SwiGLU/rotate/S8 -> fc2 (0 to skip)")
     ap.add_argument("--rows", type=int, default=0,
                     help="truncate M to this many tokens (small profiling case; not a bench line)")
     args = ap.parse_args()
@@ -529,6 +591,10 @@ def main():
         del lo
         torch.cuda.empty_cache()
 
+    ffn = None
+    if args.ffn_block:
+        ffn = time_ffn_block(dev, world, flush, args.warmup)
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         cpu = cpu_baseline(wl, args.cpu_budget)
@@ -562,6 +628,7 @@ def main():
         "cpu_baseline": cpu,
         "secondary": secondary,
         "others": others,
+        "ffn_block": ffn,
         "vs_baseline_note": "value / the pages' A40 QKV layer (25.08 ms = 184.3 TOPS): context only",
     }
     print(json.dumps(line), flush=True)

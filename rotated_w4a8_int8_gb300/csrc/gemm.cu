@@ -280,7 +280,8 @@ template <> __device__ __forceinline__ __half to_out<CONVROT_FP16>(float y) { re
 template <> __device__ __forceinline__ float to_out<CONVROT_FP32>(float y) { return y; }
 
 // OUT = CONVROT_BF16 / FP16 / FP32, or -1 for raw int32 accumulators.
-template <int OUT>
+// BIAS: p.bias is non-null and added in the epilogue.
+template <int OUT, bool BIAS>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_out, const Params p) {
@@ -495,21 +496,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                 for (int q = 0; q < VEC; q += 4) {
                   const float4 f = __ldg(reinterpret_cast<const float4*>(p.w_scale + n + q));
                   sw[q] = f.x; sw[q + 1] = f.y; sw[q + 2] = f.z; sw[q + 3] = f.w;
-                  const float4 g = p.bias ? __ldg(reinterpret_cast<const float4*>(p.bias + n + q))
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-                  bs[q] = g.x; bs[q + 1] = g.y; bs[q + 2] = g.z; bs[q + 3] = g.w;
+                  if constexpr (BIAS) {
+                    const float4 g = __ldg(reinterpret_cast<const float4*>(p.bias + n + q));
+                    bs[q] = g.x; bs[q + 1] = g.y; bs[q + 2] = g.z; bs[q + 3] = g.w;
+                  } else {
+                    bs[q] = bs[q + 1] = bs[q + 2] = bs[q + 3] = 0.f;
+                  }
                 }
               } else {
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) {
                   sw[q] = (n + q < p.N) ? __ldg(p.w_scale + n + q) : 0.f;
-                  bs[q] = (p.bias && n + q < p.N) ? __ldg(p.bias + n + q) : 0.f;
+                  bs[q] = (BIAS && n + q < p.N) ? __ldg(p.bias + n + q) : 0.f;
                 }
               }
               union { T v[VEC]; uint4 u; } pk;
 #pragma unroll
-              for (int q = 0; q < VEC; ++q)
-                pk.v[q] = to_out<OUT>(__fadd_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + q]), sa), sw[q]), bs[q]));
+              for (int q = 0; q < VEC; ++q) {
+                const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + q]), sa), sw[q]);
+                pk.v[q] = to_out<OUT>(BIAS ? __fadd_rn(y, bs[q]) : y);
+              }
               // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
               *reinterpret_cast<uint4*>(rowp + ((c ^ ((lane >> 1) & 3)) << 4)) = pk.u;
             }
@@ -530,9 +536,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
               union { T v[VEC]; uint4 u; } pk;
 #pragma unroll
               for (int j = 0; j < VEC; ++j) {
-                const float y = __fadd_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa),
-                                                    __ldg(p.w_scale + n + j)),
-                                          p.bias ? __ldg(p.bias + n + j) : 0.f);
+                float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa), __ldg(p.w_scale + n + j));
+                if constexpr (BIAS) y = __fadd_rn(y, __ldg(p.bias + n + j));
                 pk.v[j] = to_out<OUT>(y);
               }
               *reinterpret_cast<uint4*>(orow + n) = pk.u;
@@ -540,9 +545,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 #pragma unroll
               for (int j = 0; j < VEC; ++j) {
                 if (n + j < p.N) {
-                  const float y = __fadd_rn(__fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa),
-                                                      __ldg(p.w_scale + n + j)),
-                                            p.bias ? __ldg(p.bias + n + j) : 0.f);
+                  float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa), __ldg(p.w_scale + n + j));
+                  if constexpr (BIAS) y = __fadd_rn(y, __ldg(p.bias + n + j));
                   orow[n + j] = to_out<OUT>(y);
                 }
               }
@@ -621,7 +625,7 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int
 
 // Persistent grid: as many clusters as can be resident at once (one CTA per
 // SM), never more than there are pair tiles.
-template <int OUT>
+template <int OUT, bool BIAS>
 static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                           const Params& p, cudaStream_t st) {
   static int max_clusters_by_dev[64] = {0};   // resident clusters, per device and instantiation
@@ -644,14 +648,14 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     cfg.gridDim = dim3(sms / CLUSTER * CLUSTER);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<OUT>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<OUT, BIAS>, &cfg);
     if (e != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
       n = sms / CLUSTER;
@@ -660,7 +664,7 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   }
   const int clusters = p.num_pair_tiles < max_clusters ? p.num_pair_tiles : max_clusters;
   cfg.gridDim = dim3(clusters * CLUSTER);
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<OUT>, ma, mb, mo, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<OUT, BIAS>, ma, mb, mo, p);
 }
 
 static int validate_operands(const void* a_q, int64_t ld_aq, const void* w_q, int64_t ld_wq, int M,
@@ -703,11 +707,12 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.out_tma = 0;
   if (out_kind >= 0 && p.out_vec) p.out_tma = make_out_map(&mo, out, out_kind, M, N, ld_out) ? 1 : 0;
   cudaError_t e;
+  const bool b = bias != nullptr;
   switch (out_kind) {
-    case CONVROT_BF16: e = launch<CONVROT_BF16>(ma, mb, mo, p, stream); break;
-    case CONVROT_FP16: e = launch<CONVROT_FP16>(ma, mb, mo, p, stream); break;
-    case CONVROT_FP32: e = launch<CONVROT_FP32>(ma, mb, mo, p, stream); break;
-    default: e = launch<-1>(ma, mb, mo, p, stream); break;
+    case CONVROT_BF16: e = b ? launch<CONVROT_BF16, true>(ma, mb, mo, p, stream) : launch<CONVROT_BF16, false>(ma, mb, mo, p, stream); break;
+    case CONVROT_FP16: e = b ? launch<CONVROT_FP16, true>(ma, mb, mo, p, stream) : launch<CONVROT_FP16, false>(ma, mb, mo, p, stream); break;
+    case CONVROT_FP32: e = b ? launch<CONVROT_FP32, true>(ma, mb, mo, p, stream) : launch<CONVROT_FP32, false>(ma, mb, mo, p, stream); break;
+    default: e = launch<-1, false>(ma, mb, mo, p, stream); break;
   }
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("GEMM launch", e);
 }

@@ -192,27 +192,32 @@ __device__ __forceinline__ void load_act_row(const char* xrow, int K, int nblock
 }
 
 // Channel pre-scales p[c0 .. c0+31] applied to the pass-1 pairs
-// P[b] = (elem b, elem 16 + b); nothing at or past K is read.
+// P[b] = (elem b, elem 16 + b), four pairs at a time; nothing at or past K
+// is read.
 __device__ __forceinline__ void apply_pre_scale(const float* __restrict__ p, int c0, int K, float2 (&P)[16]) {
   if (c0 >= K) return;
-  float ps[32];
-  if (c0 + 32 <= K) {
+  const bool full = c0 + 32 <= K;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(p + c0) + u);
-      ps[4 * u] = f.x; ps[4 * u + 1] = f.y; ps[4 * u + 2] = f.z; ps[4 * u + 3] = f.w;
+  for (int j = 0; j < 4; ++j) {
+    float4 lo, hi;                       // elements 4j..4j+3 and 16+4j..16+4j+3
+    if (full) {
+      lo = __ldg(reinterpret_cast<const float4*>(p + c0 + 4 * j));
+      hi = __ldg(reinterpret_cast<const float4*>(p + c0 + 16 + 4 * j));
+    } else {
+      auto at = [&](int e) { return (c0 + e < K) ? __ldg(p + c0 + e) : 0.f; };
+      lo = make_float4(at(4 * j), at(4 * j + 1), at(4 * j + 2), at(4 * j + 3));
+      hi = make_float4(at(16 + 4 * j), at(17 + 4 * j), at(18 + 4 * j), at(19 + 4 * j));
     }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) ps[e] = (c0 + e < K) ? __ldg(p + c0 + e) : 0.f;
+    P[4 * j] = mul2(P[4 * j], make_float2(lo.x, hi.x));
+    P[4 * j + 1] = mul2(P[4 * j + 1], make_float2(lo.y, hi.y));
+    P[4 * j + 2] = mul2(P[4 * j + 2], make_float2(lo.z, hi.z));
+    P[4 * j + 3] = mul2(P[4 * j + 3], make_float2(lo.w, hi.w));
   }
-#pragma unroll
-  for (int b = 0; b < 16; ++b) P[b] = mul2(P[b], make_float2(ps[b], ps[16 + b]));
 }
 
 // One activation row from its raw input: (SwiGLU,) (channel pre-scale,)
 // rotation, CTA absmax, scale and codes.  `red` is this row's reduction buffer.
-template <int DT, bool SWIGLU, int NBMAX>
+template <int DT, bool SWIGLU, int NBMAX, bool PRESCALE>
 __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, int row, int K, int nblocks,
                                         int S, int slot, int lane8, char* my, float* red,
                                         const float* pre_scale, void* q, int f16_codes, int64_t ld_q,
@@ -227,7 +232,7 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
     if (active) {
       if constexpr (SWIGLU) pairs_swiglu<DT>(cur.g[i], cur.v[SWIGLU ? i : 0], P);
       else pairs_from_raw<DT>(cur.g[i], P);
-      if (pre_scale) apply_pre_scale(pre_scale, blk * kBlock + 32 * lane8, K, P);
+      if constexpr (PRESCALE) apply_pre_scale(pre_scale, blk * kBlock + 32 * lane8, K, P);
     }
     rotate_block(P, c[i], my, lane8, active);
     if (active) amax = absmax_cols(amax, c[i]);
@@ -248,7 +253,7 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
 }
 
 // Kernel 2: one CTA per activation row.
-template <int DT, bool SWIGLU, int NBMAX, int VEC>
+template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE>
 __global__ void __launch_bounds__(kMaxThreads)
 quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S,
                  const float* __restrict__ pre_scale, void* __restrict__ q, int f16_codes, int64_t ld_q,
@@ -261,8 +266,8 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nbl
   ActRaw<DT, SWIGLU, NBMAX> cur;
   load_act_row<DT, SWIGLU, NBMAX, VEC>(static_cast<const char*>(x) + static_cast<size_t>(row) * ld_x * esize,
                                        K, nblocks, S, slot, lane8, cur);
-  act_row<DT, SWIGLU, NBMAX>(cur, row, K, nblocks, S, slot, lane8, smem + slot * kSlotBytes, red, pre_scale, q,
-                             f16_codes, ld_q, scale);
+  act_row<DT, SWIGLU, NBMAX, PRESCALE>(cur, row, K, nblocks, S, slot, lane8, smem + slot * kSlotBytes, red,
+                                       pre_scale, q, f16_codes, ld_q, scale);
 }
 
 // Raw NVFP4 input of one weight row for this thread.
@@ -390,7 +395,7 @@ static cudaError_t prep_smem(Kern k, size_t smem) {
 template <int DT, bool SWIGLU, int VEC, int NB>
 static cudaError_t launch_act_nb(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
                                  const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
-  auto k = quant_act_kernel<DT, SWIGLU, NB, VEC>;
+  auto k = ps ? quant_act_kernel<DT, SWIGLU, NB, VEC, true> : quant_act_kernel<DT, SWIGLU, NB, VEC, false>;
   cudaError_t e = prep_smem(k, g.smem);
   if (e != cudaSuccess) return e;
   k<<<M, g.threads, g.smem, st>>>(x, ld_x, M, K, g.nblocks, g.S, ps, q, f16, ld_q, scale);
