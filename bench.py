@@ -400,6 +400,65 @@ def time_ffn_block(dev, world, flush, warmup, steps=10):
             "ms_per_block": ms, "eff_tops": ops / (ms / 1e3) / 1e12, "kernels_per_step": 6}
 
 
+def time_controls(wl: synth.Workload, dev, world, flush, warmup, steps=20):
+    """The pages' comparison points on the main workload, same calls:
+    - w8a8_resident_s8: weights prepared once and kept as 1-byte S8 codes,
+      widened to the GEMM's FP16 codes every call, + act quant + GEMM;
+    - resident_f16_codes: weights prepared once in the GEMM's operand format
+      (the 'expanded W8A8' control): act quant + GEMM only;
+    - prescale_bias: the full layer with channel pre-scales and a bias."""
+    import torch
+
+    import rotated_w4a8_int8_gb300 as cr
+    L = Layer(wl, dev)
+    Kp = L.sz["Kp"]
+    wq8 = torch.empty(wl.N, Kp, dtype=torch.int8, device=dev)
+    sw8 = torch.empty(wl.N, dtype=torch.float32, device=dev)
+    cr.prepare_weight(L.p, L.s, L.t, wl.K, wq8, sw8)
+    L.weight()
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    pre = torch.exp(torch.rand(wl.K, generator=gen) * 2 - 1).to(dev)
+    bias = (torch.randn(wl.N, generator=gen) * 0.1).to(dev)
+
+    def w8a8():
+        cr.widen_codes(wq8, L.wq, cols=Kp)
+        L.act()
+        L.gemm()
+
+    def resident():
+        L.act()
+        L.gemm()
+
+    def ps_bias():
+        L.weight()
+        cr.quant_act(L.x, wl.K, L.aq, L.sa, swiglu=wl.swiglu, pre_scale=pre)
+        cr.gemm(L.aq, L.sa, L.wq, L.sw, L.y, bias=bias)
+
+    out = {}
+    for name, fn in (("w8a8_resident_s8", w8a8), ("resident_f16_codes", resident), ("prescale_bias", ps_bias)):
+        for _ in range(warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        tot = 0.0
+        for _ in range(steps):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        ms = reduce_max(tot, world) / steps
+        out[name] = {"ms_per_layer": ms, "eff_tops": L.sz["ops"] / (ms / 1e3) / 1e12}
+    out["pages_a40_ms"] = {"w8a8_expanded": 23.40, "convrot_w4a8": 25.08}
+    del L
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------- CPU oracle baseline
 class OracleSample:
     """The first m tokens x first n weight rows of a workload, generated once;
@@ -485,6 +544,8 @@ def main():
     ap.add_argument("--others", default="ffn_up,ragged,wide_k",
                     help="further workloads timed briefly in the same run ('' to skip)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--controls", type=int, default=1,
+                    help="also time the W8A8 / resident-weight controls and pre-scale+bias (0 to skip)")
     ap.add_argument("--ffn-block", type=int, default=1,
                     help="also time the FFN block fc1 -> SwiGLU/rotate/S8 -> fc2 (0 to skip)")
     ap.add_argument("--rows", type=int, default=0,
@@ -594,6 +655,9 @@ def main():
     ffn = None
     if args.ffn_block:
         ffn = time_ffn_block(dev, world, flush, args.warmup)
+    controls = None
+    if args.controls:
+        controls = time_controls(wl, dev, world, flush, args.warmup)
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
@@ -629,6 +693,7 @@ def main():
         "secondary": secondary,
         "others": others,
         "ffn_block": ffn,
+        "controls": controls,
         "vs_baseline_note": "value / the pages' A40 QKV layer (25.08 ms = 184.3 TOPS): context only",
     }
     print(json.dumps(line), flush=True)

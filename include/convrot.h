@@ -154,6 +154,19 @@ int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale,
                  cudaStream_t stream);
 
 /*
+ * W8A8 with resident weights: widens S8 codes (CONVROT_CODES_S8, e.g. weight
+ * codes prepared once and kept at one byte each) into the FP16-held codes
+ * that convrot_gemm reads (the page's "W8A8 controls use the same
+ * NVFP4-derived rotated S8 weights").
+ *
+ *   src  [rows][ld_src] int8, 16-byte aligned, ld_src a multiple of 16.
+ *   dst  [rows][ld_dst] FP16, 16-byte aligned, ld_dst a multiple of 8.
+ *   cols a multiple of 16; columns 0..cols-1 are converted exactly.
+ */
+int convrot_widen_codes(const int8_t* src, int64_t ld_src, int rows, int cols,
+                        void* dst, int64_t ld_dst, cudaStream_t stream);
+
+/*
  * Test hook: the same GEMM, writing the raw int32 accumulators
  * acc[m, n] = sum_k q_a[m, k] * q_w[n, k] into acc [M][ld_acc] instead of
  * dequantising.  Arguments and rules as convrot_gemm.

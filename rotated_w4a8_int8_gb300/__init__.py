@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "load_library", "padded_k", "status_string", "last_error", "prepare_weight", "quant_act", "gemm",
-    "gemm_i32", "gemm_timeout_selftest", "device_error", "ConvRotError", "BF16", "FP16", "FP32", "CODES_S8",
+    "gemm_i32", "widen_codes", "gemm_timeout_selftest", "device_error", "ConvRotError", "BF16", "FP16", "FP32", "CODES_S8",
     "CODES_F16", "LIB_PATH", "EXPORTS",
 ]
 
@@ -23,7 +23,7 @@ BF16, FP16, FP32 = 0, 1, 2
 CODES_S8, CODES_F16 = 0, 1
 EXPORTS = ("convrot_padded_k", "convrot_status_string", "convrot_prepare_weight",
            "convrot_quant_act", "convrot_gemm", "convrot_gemm_i32", "convrot_device_error",
-           "convrot_last_error", "convrot_gemm_timeout_selftest")
+           "convrot_last_error", "convrot_gemm_timeout_selftest", "convrot_widen_codes")
 
 _lib = None
 
@@ -57,6 +57,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.convrot_gemm.restype = i32
     lib.convrot_gemm_i32.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp, i64, vp]
     lib.convrot_gemm_i32.restype = i32
+    lib.convrot_widen_codes.argtypes = [vp, i64, i32, i32, vp, i64, vp]
+    lib.convrot_widen_codes.restype = i32
     lib.convrot_gemm_timeout_selftest.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp, i64, vp]
     lib.convrot_gemm_timeout_selftest.restype = i32
     lib.convrot_last_error.argtypes = []
@@ -142,6 +144,14 @@ def gemm_i32(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:
     _check("convrot_gemm_i32", load_library().convrot_gemm_i32(
         _ptr(a_q), a_q.stride(0), _ptr(w_q), w_q.stride(0), M, N, int(K_p), _ptr(acc),
         acc.stride(0), _stream(stream)))
+
+
+def widen_codes(src, dst, cols: int | None = None, stream=None) -> None:
+    """convrot_widen_codes: int8 S8 codes [rows, >=cols] -> float16 codes [rows, >=cols]."""
+    rows = src.shape[0]
+    cols = src.shape[1] if cols is None else cols
+    _check("convrot_widen_codes", load_library().convrot_widen_codes(
+        _ptr(src), src.stride(0), rows, int(cols), _ptr(dst), dst.stride(0), _stream(stream)))
 
 
 def gemm_timeout_selftest(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:

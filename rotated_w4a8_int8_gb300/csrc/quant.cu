@@ -1,14 +1,16 @@
 // Kernels 1 and 2 of the ConvRot W4A8 layer and their C-ABI entry points.
 //
 //   convrot_prepare_weight: NVFP4 decode -> ConvRot256 rotation (FP32) -> row S8
-//   convrot_quant_act:      (SwiGLU ->) ConvRot256 rotation (FP32) -> row S8
+//   convrot_quant_act:      (SwiGLU ->) (channel pre-scale ->) ConvRot256
+//                           rotation (FP32) -> row S8
 //
 // Both follow the ComfyUI Turing Utils page (comfy.icu), node list, entry
 // "Load ConvRot DiT and Load ConvRot CLIP also accept ComfyUI-native nvfp4
 // layers": paired ConvRot256 on activations and decoded NVFP4 weights, both
 // operands zero-padded to whole 256-blocks, FP32 rotation, row-scaled S8 with
-// a rounded FP32 scale reciprocal.  SwiGLU follows the MiniMax-H3 explainer
-// (modelpad.app), MLP section: gate, value = chunk(2); swish(gate) * value.
+// a rounded FP32 scale reciprocal; pre-scales and SwiGLU before the rotation.
+// SwiGLU follows the MiniMax-H3 explainer (modelpad.app), MLP section:
+// gate, value = chunk(2); swish(gate) * value.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
@@ -519,4 +521,51 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
     default: e = launch_weight_w<4>(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
   }
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("prepare_weight launch", e);
+}
+
+// ------------------------------------------------------------------ S8 -> FP16 code widening
+// W8A8 with resident weights (the page's "W8A8 controls use the same
+// NVFP4-derived rotated S8 weights"): weights kept as 1-byte S8 codes are
+// widened to the FP16-held codes the GEMM reads.  Each thread converts 16
+// codes (one 16-byte load, two 16-byte stores); rows and pitches must keep
+// those accesses aligned.
+namespace convrot {
+__global__ void __launch_bounds__(256)
+widen_codes_kernel(const int8_t* __restrict__ src, int64_t ld_src, int rows, int cols,
+                   __half* __restrict__ dst, int64_t ld_dst) {
+  const int per_row = cols / 16;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(rows) * per_row) return;
+  const int r = static_cast<int>(i / per_row), c = static_cast<int>(i % per_row) * 16;
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + r * ld_src + c));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t word = w[j >> 1] >> (16 * (j & 1));
+    const int lo = static_cast<int8_t>(word & 0xffu), hi = static_cast<int8_t>((word >> 8) & 0xffu);
+    const __half2 p = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+    h[j] = *reinterpret_cast<const uint32_t*>(&p);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst + r * ld_dst + c);
+  d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+}  // namespace convrot
+
+extern "C" int convrot_widen_codes(const int8_t* src, int64_t ld_src, int rows, int cols, void* dst,
+                                   int64_t ld_dst, cudaStream_t stream) {
+  if (rows < 0 || cols < 0 || cols % 16 || ld_src < cols || ld_dst < cols) return CONVROT_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return CONVROT_OK;
+  if (!src || !dst) return CONVROT_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16 || ld_src % 16 ||
+      ld_dst % 8)
+    return CONVROT_ERR_MISALIGNED;
+  const int64_t n = static_cast<int64_t>(rows) * (cols / 16);
+  const int64_t blocks = (n + 255) / 256;
+  if (blocks > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  widen_codes_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, ld_src, rows, cols,
+                                                                        static_cast<__half*>(dst), ld_dst);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("widen_codes launch", e);
 }

@@ -105,3 +105,14 @@ def test_binding_fails_loudly_without_library(tmp_path):
             cr.load_library(str(tmp_path / "missing.so"))
     finally:
         cr._lib = saved
+
+
+def test_widen_codes_rejects_bad_arguments(lib):
+    f = lib.convrot_widen_codes
+    P = 1 << 20
+    assert f(P, 64, 4, 40, P, 64, 0) == 1           # cols not a multiple of 16
+    assert f(P, 32, 4, 48, P, 64, 0) == 1           # ld_src < cols
+    assert f(P + 8, 64, 4, 48, P, 64, 0) == 2       # src not 16-byte aligned
+    assert f(P, 64, 4, 48, P, 60, 0) == 2           # ld_dst not a multiple of 8
+    assert f(None, 64, 4, 48, P, 64, 0) == 1
+    assert f(P, 64, 0, 48, P, 64, 0) == 0           # empty

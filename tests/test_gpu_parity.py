@@ -275,3 +275,34 @@ def test_layer_with_channel_pre_scale_and_bias(case, wl):
     assert_codes_match(codes_to_np(qa, Kp), mid["qa"])
     assert_scales_match(sa.cpu().numpy(), mid["sa"])
     assert_output_match(y.float().cpu().numpy(), ref)
+
+
+def test_widen_codes_is_exact():
+    import rotated_w4a8_int8_gb300 as cr
+    rng = np.random.default_rng(51)
+    src = rng.integers(-128, 128, (37, 272)).astype(np.int8)
+    src[0, :255] = np.arange(-127, 128)
+    s = torch.from_numpy(src).to(DEV)
+    d = torch.full((37, 280), 7.0, dtype=torch.float16, device=DEV)
+    cr.widen_codes(s, d, cols=272)
+    got = d.cpu().numpy()
+    assert np.array_equal(got[:, :272].astype(np.int32), src.astype(np.int32))
+    assert np.all(got[:, 272:] == 7.0)
+
+
+def test_w8a8_resident_s8_weights_match_the_w4a8_layer():
+    # weights prepared once into S8 storage, widened per call: same outputs
+    import rotated_w4a8_int8_gb300 as cr
+    wl = small("qkv", 200, 300)
+    x = synth.make_activations(wl)
+    packed, scales, t = synth.make_nvfp4_weight(wl)
+    Kp = oracle.padded_k(wl.K)
+    q16, sw = gpu_prepare_weight(packed, scales, t, wl.K, fmt="f16")
+    q8, sw8 = gpu_prepare_weight(packed, scales, t, wl.K, fmt="s8")
+    wide = torch.empty(wl.N, Kp, dtype=torch.float16, device=DEV)
+    cr.widen_codes(q8, wide, cols=Kp)
+    assert torch.equal(wide, q16) and torch.equal(sw8, sw)
+    qa, sa = gpu_quant_act(x, wl.x_dtype, wl.K)
+    y1 = gpu_gemm(qa, sa, q16, sw, "bf16", Kp)
+    y2 = gpu_gemm(qa, sa, wide, sw8, "bf16", Kp)
+    assert torch.equal(y1, y2)
