@@ -91,6 +91,7 @@ const char* convrot_status_string(int status);
  * s_w = fp32(max|r| / 127); q = clamp(rint(r * fp32(1/s_w)), -127, 127), the
  * product and rounding done in FP32 (half to even).  A row whose s_w is 0 or
  * whose reciprocal overflows is written as all-zero codes with s_w = 0.
+ * A row holding an Inf or NaN value gets unspecified codes and scale.
  * Alignment: w_fp4 8-byte aligned; w_q 4-byte (F16 codes) or 2-byte (S8
  * codes) aligned with ld_wq even (codes are written in pairs).
  */
@@ -117,7 +118,8 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
  *   a_scale [M] FP32 token scales s_a (0 for a degenerate row).
  *
  * Quantiser as for the weights (FP32 scale, FP32 reciprocal, FP32 product,
- * round half to even, clamp to +-127).  FP16 inputs are widened to FP32
+ * round half to even, clamp to +-127).  A row holding an Inf or NaN value
+ * gets unspecified codes and scale.  FP16 inputs are widened to FP32
  * before anything else.  x needs only element alignment; rows aligned to 32
  * or 16 bytes take the vectorised load paths.  a_q is 4-byte (F16 codes) or
  * 2-byte (S8 codes) aligned with ld_aq even (codes are written in pairs).

@@ -26,11 +26,13 @@
 // CTAs, so every SM pulls 32 KiB instead of 48 KiB from L2 per K step.  A
 // stage is refilled only after the MMAs of both CTAs have released it.
 // Clusters are persistent over a grouped tile order.  Warp 0: TMA producer.
-// Warp 1: TMEM owner and MMA issuer.  Warps 2..9: epilogue.  Every mbarrier
-// wait is bounded: after about two seconds the waiting role records an error
-// code, the CTA drains what it has in flight and returns.
+// Warp 1: TMEM owner and MMA issuer.  Warps 2..9: epilogue, which applies
+// y = fp32(acc) * s_a * s_w (+ bias), stages 32-row x 64-byte boxes in
+// swizzled shared memory and writes them with TMA tensor stores (per-element
+// stores for unaligned outputs).  Every mbarrier wait is bounded: after about
+// two seconds the waiting role records an error code, the CTA drains what it
+// has in flight and returns.
 #include <cstdint>
-#include <cstdio>
 #include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -63,8 +65,9 @@ constexpr int OUT_STAGING = NUM_EPI_WARPS * 2 * OUT_BOX;     // 32 KiB
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// Codes recorded in g_error: which wait ran out first.
 enum ErrCode : int { ERR_NONE = 0, ERR_WAIT_FULL = 1, ERR_WAIT_EMPTY = 2, ERR_WAIT_ACC_FULL = 3,
-                     ERR_WAIT_ACC_EMPTY = 4, ERR_WAIT_DRAIN = 5 };
+                     ERR_WAIT_ACC_EMPTY = 4 };
 
 __device__ int g_error = 0;   // first failure code of any GEMM launch (0 = none)
 

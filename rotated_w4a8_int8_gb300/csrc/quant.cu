@@ -179,14 +179,14 @@ struct ActRaw {
 };
 
 template <int DT, bool SWIGLU, int NBMAX, int VEC>
-__device__ __forceinline__ void load_act_row(const char* xrow, int K, int nblocks, int S, int slot,
+__device__ __forceinline__ void load_act_row(const char* xrow, int K, int blk0, int nloc, int S, int slot,
                                              int lane8, ActRaw<DT, SWIGLU, NBMAX>& r) {
   constexpr size_t esize = (DT == DT_FP32) ? 4 : 2;
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
-    const int blk = slot + S * i;
-    if (slot < S && blk < nblocks) {
-      const int c0 = blk * kBlock + 32 * lane8;
+    const int li = slot + S * i;
+    if (slot < S && li < nloc) {
+      const int c0 = (blk0 + li) * kBlock + 32 * lane8;
       load_raw<DT, VEC>(xrow, c0, K, r.g[i]);
       if constexpr (SWIGLU) load_raw<DT, VEC>(xrow + static_cast<size_t>(K) * esize, c0, K, r.v[i]);
     }
@@ -219,17 +219,17 @@ __device__ __forceinline__ void apply_pre_scale(const float* __restrict__ p, int
 
 // One activation row from its raw input: (SwiGLU,) (channel pre-scale,)
 // rotation, CTA absmax, scale and codes.  `red` is this row's reduction buffer.
-template <int DT, bool SWIGLU, int NBMAX, bool PRESCALE>
-__device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, int row, int K, int nblocks,
-                                        int S, int slot, int lane8, char* my, float* red,
-                                        const float* pre_scale, void* q, int f16_codes, int64_t ld_q,
-                                        float* scale) {
+template <int DT, bool SWIGLU, int NBMAX, bool PRESCALE, int SPLIT>
+__device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, int row, int K, int blk0,
+                                        int nloc, int S, int slot, int lane8, char* my, float* red,
+                                        float* xred, const float* pre_scale, void* q, int f16_codes,
+                                        int64_t ld_q, float* scale) {
   BlockCols c[NBMAX];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
-    const int blk = slot + S * i;
-    const bool active = (slot < S) && (blk < nblocks);
+    const int li = slot + S * i, blk = blk0 + li;
+    const bool active = (slot < S) && (li < nloc);
     float2 P[16];
     if (active) {
       if constexpr (SWIGLU) pairs_swiglu<DT>(cur.g[i], cur.v[SWIGLU ? i : 0], P);
@@ -240,36 +240,43 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
     if (active) amax = absmax_cols(amax, c[i]);
   }
   // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
-  const RowQuant rq(cta_absmax(amax, red) * 0.0625f);
-  if (threadIdx.x == 0) scale[row] = rq.s;
+  float zmax = cta_absmax(amax, red);
+  if constexpr (SPLIT == 2) zmax = cluster_pair_absmax(zmax, xred);
+  const RowQuant rq(zmax * 0.0625f);
+  if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
   const float mult = rq.r * 0.0625f;           // fp32(z * (r / 16)) == fp32((z / 16) * r)
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
-    const int blk = slot + S * i;
-    if (slot < S && blk < nblocks) {
+    const int li = slot + S * i;
+    if (slot < S && li < nloc) {
       scale_cols(c[i], mult);
-      store_codes(qrow, f16_codes, blk, lane8, c[i]);
+      store_codes(qrow, f16_codes, blk0 + li, lane8, c[i]);
     }
   }
 }
 
-// Kernel 2: one CTA per activation row.
-template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE>
+// Kernel 2: one CTA per activation row, or (SPLIT == 2) a cluster of two
+// CTAs per row, each owning half of the row's blocks.
+template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE, int SPLIT>
 __global__ void __launch_bounds__(kMaxThreads)
 quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S,
                  const float* __restrict__ pre_scale, void* __restrict__ q, int f16_codes, int64_t ld_q,
                  float* __restrict__ scale) {
   extern __shared__ __align__(16) char smem[];
   float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);   // per-warp maxima
+  float* xred = red + kMaxThreads / 32;                           // cluster exchange slot
   const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
   constexpr size_t esize = (DT == DT_FP32) ? 4 : 2;
-  const int row = blockIdx.x;
+  const int row = blockIdx.x / SPLIT, part = blockIdx.x % SPLIT;
+  const int nbl = (nblocks + SPLIT - 1) / SPLIT;
+  const int blk0 = part * nbl, nloc = min(nbl, nblocks - blk0);
   ActRaw<DT, SWIGLU, NBMAX> cur;
   load_act_row<DT, SWIGLU, NBMAX, VEC>(static_cast<const char*>(x) + static_cast<size_t>(row) * ld_x * esize,
-                                       K, nblocks, S, slot, lane8, cur);
-  act_row<DT, SWIGLU, NBMAX, PRESCALE>(cur, row, K, nblocks, S, slot, lane8, smem + slot * kSlotBytes, red,
-                                       pre_scale, q, f16_codes, ld_q, scale);
+                                       K, blk0, nloc, S, slot, lane8, cur);
+  act_row<DT, SWIGLU, NBMAX, PRESCALE, SPLIT>(cur, row, K, blk0, nloc, S, slot, lane8, smem + slot * kSlotBytes,
+                                              red, xred, pre_scale, q, f16_codes, ld_q, scale);
+  if constexpr (SPLIT == 2) cluster_exit_wait();
 }
 
 // Raw NVFP4 input of one weight row for this thread.
@@ -307,30 +314,30 @@ __device__ __forceinline__ void load_nvfp4_raw(const uint8_t* prow, const uint8_
 
 template <int NBMAX, bool W16>
 __device__ __forceinline__ void load_weight_row(const uint8_t* w_fp4, const uint8_t* w_sf, int row, int K,
-                                                int K_s, int nblocks, int S, int slot, int lane8,
+                                                int K_s, int blk0, int nloc, int S, int slot, int lane8,
                                                 WRaw<NBMAX>& r) {
   const uint8_t* prow = w_fp4 + static_cast<size_t>(row) * (K_s >> 1);
   const uint8_t* srow = w_sf + static_cast<size_t>(row) * (K_s >> 4);
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
-    const int blk = slot + S * i;
-    if (slot < S && blk < nblocks)
-      load_nvfp4_raw<W16>(prow, srow, blk * kBlock + 32 * lane8, K, K_s, r.w0[i], r.w1[i], r.sc[i]);
+    const int li = slot + S * i;
+    if (slot < S && li < nloc)
+      load_nvfp4_raw<W16>(prow, srow, (blk0 + li) * kBlock + 32 * lane8, K, K_s, r.w0[i], r.w1[i], r.sc[i]);
   }
 }
 
 // One weight row from its raw input: decode, rotation, tensor scale, CTA
 // absmax, scale and codes.
-template <int NBMAX>
-__device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K, int nblocks, int S, int slot,
-                                           int lane8, float t16, char* my, float* red, void* q, int f16_codes,
-                                           int64_t ld_q, float* scale) {
+template <int NBMAX, int SPLIT>
+__device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K, int blk0, int nloc, int S,
+                                           int slot, int lane8, float t16, char* my, float* red, float* xred,
+                                           void* q, int f16_codes, int64_t ld_q, float* scale) {
   BlockCols c[NBMAX];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
-    const int blk = slot + S * i;
-    const bool active = (slot < S) && (blk < nblocks);
+    const int li = slot + S * i, blk = blk0 + li;
+    const bool active = (slot < S) && (li < nloc);
     float2 P[16];
     if (active) decode_nvfp4_pairs(r.w0[i], r.w1[i], r.sc[i], blk * kBlock + 32 * lane8, K, P);
     rotate_block(P, c[i], my, lane8, active);
@@ -339,52 +346,70 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
       amax = absmax_cols(amax, c[i]);
     }
   }
-  const RowQuant rq(cta_absmax(amax, red));
-  if (threadIdx.x == 0) scale[row] = rq.s;
+  float wmax = cta_absmax(amax, red);
+  if constexpr (SPLIT == 2) wmax = cluster_pair_absmax(wmax, xred);
+  const RowQuant rq(wmax);
+  if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
-    const int blk = slot + S * i;
-    if (slot < S && blk < nblocks) {
+    const int li = slot + S * i;
+    if (slot < S && li < nloc) {
       scale_cols(c[i], rq.r);
-      store_codes(qrow, f16_codes, blk, lane8, c[i]);
+      store_codes(qrow, f16_codes, blk0 + li, lane8, c[i]);
     }
   }
 }
 
-// Kernel 1: one CTA per weight row.
-template <int NBMAX, bool W16>
+// Kernel 1: one CTA per weight row, or (SPLIT == 2) a cluster of two CTAs
+// per row, each owning half of the row's blocks.
+template <int NBMAX, bool W16, int SPLIT>
 __global__ void __launch_bounds__(kMaxThreads)
 prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restrict__ w_sf,
                       const float* __restrict__ tscale, int N, int K, int K_s, int nblocks, int S,
                       void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
   extern __shared__ __align__(16) char smem[];
   float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);
+  float* xred = red + kMaxThreads / 32;
   const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
   const float t16 = __ldg(tscale) * 0.0625f;  // t / 16 is exact
-  const int row = blockIdx.x;
+  const int row = blockIdx.x / SPLIT, part = blockIdx.x % SPLIT;
+  const int nbl = (nblocks + SPLIT - 1) / SPLIT;
+  const int blk0 = part * nbl, nloc = min(nbl, nblocks - blk0);
   WRaw<NBMAX> r0;
-  load_weight_row<NBMAX, W16>(w_fp4, w_sf, row, K, K_s, nblocks, S, slot, lane8, r0);
-  weight_row<NBMAX>(r0, row, K, nblocks, S, slot, lane8, t16, smem + slot * kSlotBytes, red, q, f16_codes,
-                    ld_q, scale);
+  load_weight_row<NBMAX, W16>(w_fp4, w_sf, row, K, K_s, blk0, nloc, S, slot, lane8, r0);
+  weight_row<NBMAX, SPLIT>(r0, row, K, blk0, nloc, S, slot, lane8, t16, smem + slot * kSlotBytes, red, xred, q,
+                           f16_codes, ld_q, scale);
+  if constexpr (SPLIT == 2) cluster_exit_wait();
 }
 
 // ------------------------------------------------------------------ launch geometry
 struct RowGeometry {
-  int nblocks, nbmax, S, threads;
+  int nblocks;     // 256-blocks per row
+  int split;       // CTAs per row (1, or 2 in a cluster)
+  int nbmax;       // blocks per slot (1 or 2)
+  int S;           // slots (8 threads each) per CTA
+  int threads;
   size_t smem;
 };
 
-// At most 64 slots (512 threads) per row; each slot rotates ceil(nblocks/64)
-// blocks, held in registers (NBMAX = 1, 2 or 4 -> K_p <= 65536).
-static bool row_geometry(int K_p, RowGeometry* g) {
+// Rows of more than `split_above` blocks go to two CTAs of a cluster, each
+// with half of the blocks; otherwise one CTA holds the row.  A slot takes
+// one block, or two when a CTA's share exceeds 64 blocks (K_p <= 65536).
+// Splitting halves a row's latency but, at one block per slot, holds fewer
+// rows per SM than two blocks per slot: the activation rows gain from it
+// above 64 blocks, the shorter weight rows only where two blocks per slot
+// no longer fit one CTA (above 128).
+static bool row_geometry(int K_p, int split_above, RowGeometry* g) {
   g->nblocks = K_p / kBlock;
-  const int nb = (g->nblocks + kMaxSlots - 1) / kMaxSlots;
-  if (nb > 4) return false;
-  g->nbmax = nb <= 1 ? 1 : nb <= 2 ? 2 : 4;
-  g->S = (g->nblocks + nb - 1) / nb;
+  g->split = g->nblocks > split_above ? 2 : 1;
+  const int nbl = (g->nblocks + g->split - 1) / g->split;
+  const int nb = (nbl + kMaxSlots - 1) / kMaxSlots;
+  if (nb > 2) return false;
+  g->nbmax = nb;
+  g->S = (nbl + nb - 1) / nb;
   g->threads = ((kSlotThreads * g->S + 31) / 32) * 32;
-  g->smem = static_cast<size_t>(g->S) * kSlotBytes + (kMaxThreads / 32) * sizeof(float);
+  g->smem = static_cast<size_t>(g->S) * kSlotBytes + (kMaxThreads / 32 + 4) * sizeof(float);
   return true;
 }
 
@@ -394,24 +419,44 @@ static cudaError_t prep_smem(Kern k, size_t smem) {
   return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }
 
-template <int DT, bool SWIGLU, int VEC, int NB>
-static cudaError_t launch_act_nb(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
-                                 const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
-  auto k = ps ? quant_act_kernel<DT, SWIGLU, NB, VEC, true> : quant_act_kernel<DT, SWIGLU, NB, VEC, false>;
+// Launches `k` over `rows` rows: one CTA per row, or clusters of two.
+template <typename Kern, typename... Args>
+static cudaError_t launch_rows(Kern k, const RowGeometry& g, int rows, cudaStream_t st, Args... args) {
   cudaError_t e = prep_smem(k, g.smem);
   if (e != cudaSuccess) return e;
-  k<<<M, g.threads, g.smem, st>>>(x, ld_x, M, K, g.nblocks, g.S, ps, q, f16, ld_q, scale);
-  return cudaGetLastError();
+  if (g.split == 1) {
+    k<<<rows, g.threads, g.smem, st>>>(args...);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(rows) * 2u);
+  cfg.blockDim = dim3(g.threads);
+  cfg.dynamicSmemBytes = g.smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+template <int DT, bool SWIGLU, int VEC, int NB, int SPLIT>
+static cudaError_t launch_act_cfg(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
+                                  const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
+  auto k = ps ? quant_act_kernel<DT, SWIGLU, NB, VEC, true, SPLIT>
+              : quant_act_kernel<DT, SWIGLU, NB, VEC, false, SPLIT>;
+  return launch_rows(k, g, M, st, x, ld_x, M, K, g.nblocks, g.S, ps, q, f16, ld_q, scale);
 }
 
 template <int DT, bool SWIGLU, int VEC>
 static cudaError_t launch_act_dt(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
                                  const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
-  switch (g.nbmax) {
-    case 1: return launch_act_nb<DT, SWIGLU, VEC, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-    case 2: return launch_act_nb<DT, SWIGLU, VEC, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-    default: return launch_act_nb<DT, SWIGLU, VEC, 4>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-  }
+  if (g.split == 1) return launch_act_cfg<DT, SWIGLU, VEC, 1, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+  if (g.nbmax == 1) return launch_act_cfg<DT, SWIGLU, VEC, 1, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+  return launch_act_cfg<DT, SWIGLU, VEC, 2, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
 }
 
 template <int DT>
@@ -432,23 +477,23 @@ static cudaError_t launch_act(const RowGeometry& g, int M, const void* x, int64_
   }
 }
 
-template <int NB, bool W16>
-static cudaError_t launch_weight_nb(const RowGeometry& g, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
-                                    const float* t, int K, int K_s, void* q, int f16, int64_t ld_q,
-                                    float* scale, cudaStream_t st) {
-  auto k = prepare_weight_kernel<NB, W16>;
-  cudaError_t e = prep_smem(k, g.smem);
-  if (e != cudaSuccess) return e;
-  k<<<N, g.threads, g.smem, st>>>(w_fp4, w_sf, t, N, K, K_s, g.nblocks, g.S, q, f16, ld_q, scale);
-  return cudaGetLastError();
+template <bool W16, int NB, int SPLIT>
+static cudaError_t launch_weight_cfg(const RowGeometry& g, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
+                                     const float* t, int K, int K_s, void* q, int f16, int64_t ld_q,
+                                     float* scale, cudaStream_t st) {
+  return launch_rows(prepare_weight_kernel<NB, W16, SPLIT>, g, N, st, w_fp4, w_sf, t, N, K, K_s, g.nblocks,
+                     g.S, q, f16, ld_q, scale);
 }
 
-template <int NB>
-static cudaError_t launch_weight_w(const RowGeometry& g, bool w16, int N, const uint8_t* w_fp4,
-                                   const uint8_t* w_sf, const float* t, int K, int K_s, void* q, int f16,
-                                   int64_t ld_q, float* scale, cudaStream_t st) {
-  return w16 ? launch_weight_nb<NB, true>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st)
-             : launch_weight_nb<NB, false>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
+template <bool W16>
+static cudaError_t launch_weight(const RowGeometry& g, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
+                                 const float* t, int K, int K_s, void* q, int f16, int64_t ld_q, float* scale,
+                                 cudaStream_t st) {
+  if (g.split == 1)
+    return g.nbmax == 1 ? launch_weight_cfg<W16, 1, 1>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st)
+                        : launch_weight_cfg<W16, 2, 1>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
+  if (g.nbmax == 1) return launch_weight_cfg<W16, 1, 2>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
+  return launch_weight_cfg<W16, 2, 2>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
 }
 
 }  // namespace convrot
@@ -481,7 +526,7 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
   };
   const int vec = aligned(32) ? 2 : aligned(16) ? 1 : 0;
   RowGeometry g;
-  if (!row_geometry(K_p, &g)) return CONVROT_ERR_UNSUPPORTED;
+  if (!row_geometry(K_p, kMaxSlots, &g)) return CONVROT_ERR_UNSUPPORTED;
   const int f16 = fmt == CONVROT_CODES_F16;
   cudaError_t e;
   switch (x_dtype) {
@@ -509,17 +554,14 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
   if (reinterpret_cast<uintptr_t>(w_q) % (fmt == CONVROT_CODES_F16 ? 4 : 2) || ld_wq % 2)
     return CONVROT_ERR_MISALIGNED;
   RowGeometry g;
-  if (!row_geometry(K_p, &g)) return CONVROT_ERR_UNSUPPORTED;
+  if (!row_geometry(K_p, 2 * kMaxSlots, &g)) return CONVROT_ERR_UNSUPPORTED;
   const int K_s = ((K + 15) / 16) * 16;
   const int f16 = fmt == CONVROT_CODES_F16;
   cudaError_t e;
   // one 16-byte load per thread when every packed row starts 16-byte aligned
   const bool w16 = (reinterpret_cast<uintptr_t>(w_fp4) % 16 == 0) && ((K_s / 2) % 16 == 0);
-  switch (g.nbmax) {
-    case 1: e = launch_weight_w<1>(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
-    case 2: e = launch_weight_w<2>(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
-    default: e = launch_weight_w<4>(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream); break;
-  }
+  e = w16 ? launch_weight<true>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream)
+          : launch_weight<false>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream);
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("prepare_weight launch", e);
 }
 

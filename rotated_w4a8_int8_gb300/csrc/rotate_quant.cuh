@@ -157,6 +157,31 @@ __device__ __forceinline__ float cta_absmax(float local, float* red) {
   return m;
 }
 
+// Row absmax when a row is split over the two CTAs of a cluster: each CTA
+// holds its partial maximum (already reduced over the CTA); the two partials
+// are exchanged through distributed shared memory.  `xred` is this CTA's
+// exchange slot.  Every thread of both CTAs must call it; afterwards each
+// thread must call cluster_exit_wait() once before the CTA exits.
+__device__ __forceinline__ float cluster_pair_absmax(float cta_max, float* xred) {
+  if (threadIdx.x == 0) *xred = cta_max;
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  uint32_t rank, local = static_cast<uint32_t>(__cvta_generic_to_shared(xred)), remote;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank ^ 1u));
+  float peer;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(peer) : "r"(remote) : "memory");
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");   // done reading the peer
+  return fmaxf(cta_max, peer);
+}
+
+// Completes cluster_pair_absmax: the peer may read this CTA's slot until here.
+__device__ __forceinline__ void cluster_exit_wait() {
+  __syncwarp();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // FP32 quantiser shared by both operands, for a row of rotated values v:
 // s = fp32(amax / 127), r = fp32(1 / s), code = rint(fp32(v * r)) (half to
 // even).  |v| <= amax bounds |v * r| by 127 * (1 + 3 * 2^-24), so the code
@@ -176,11 +201,22 @@ struct RowQuant {
   }
 };
 
-__device__ __forceinline__ float rint_f(float v) {
-  float d;
-  asm("cvt.rni.f32.f32 %0, %1;" : "=f"(d) : "f"(v));
-  return d;
-}
+// Round half to even, for |v| < 2^22.  Adding 1.5 * 2^23 moves v to where
+// the FP32 spacing is 1, so the (nearest-even) add itself rounds v to an
+// integer, and subtracting the constant back is exact.  The bit pattern of
+// the sum is 0x4B400000 + code, so its low byte is the two's-complement S8
+// code.  __fadd_rn / __fsub_rn are never contracted into a multiply-add with
+// the product before them (that would round the exact product instead of the
+// FP32 one).  The adds run on the FP32 pipe; a cvt.rni conversion goes to a
+// pipe with an eighth of its rate (16 per clock per SM, measured), which the
+// SwiGLU prologue's exponentials and reciprocals already load.
+constexpr float kRoundMagic = 12582912.0f;
+
+__device__ __forceinline__ float round_magic(float v) { return __fadd_rn(v, kRoundMagic); }
+
+__device__ __forceinline__ float rint_f(float v) { return __fsub_rn(round_magic(v), kRoundMagic); }
+
+__device__ __forceinline__ uint32_t code_byte(float v) { return __float_as_uint(round_magic(v)) & 0xffu; }
 
 // Writes the codes of one block: values (already multiplied by r, so only
 // the rounding is left) for rows 2p, 2p+1 and columns 2q, 2q+1.
@@ -188,8 +224,6 @@ __device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk
                                             const BlockCols& c) {
   const int col = blk * kBlock + 2 * lane8;
   if (f16_codes) {
-    // rint on the FP32 product itself (cvt.rni): a magic-number add would let
-    // the compiler fuse it with the preceding multiply, rounding once instead
     __half2* q = reinterpret_cast<__half2*>(static_cast<__half*>(q_row) + col);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
@@ -200,10 +234,8 @@ __device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk
     uint16_t* q = reinterpret_cast<uint16_t*>(static_cast<int8_t*>(q_row) + col);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-      const int a0 = __float2int_rn(c.U[p].x), b0 = __float2int_rn(c.V[p].x);
-      const int a1 = __float2int_rn(c.U[p].y), b1 = __float2int_rn(c.V[p].y);
-      q[(32 * p) / 2] = static_cast<uint16_t>((a0 & 0xff) | ((b0 & 0xff) << 8));
-      q[(32 * p + 16) / 2] = static_cast<uint16_t>((a1 & 0xff) | ((b1 & 0xff) << 8));
+      q[(32 * p) / 2] = static_cast<uint16_t>(code_byte(c.U[p].x) | (code_byte(c.V[p].x) << 8));
+      q[(32 * p + 16) / 2] = static_cast<uint16_t>(code_byte(c.U[p].y) | (code_byte(c.V[p].y) << 8));
     }
   }
 }

@@ -97,6 +97,61 @@ def test_quant_act_degenerate_rows():
     assert_scales_match(sc, rs)
 
 
+def _fp32_tie_rows(rows, nblocks, seed):
+    """FP32 rows whose quantiser products land exactly on k + 1/2.
+
+    Block 0 of each row holds one value 16 A, so its rotated entries are all A
+    (the row maximum).  Every other block holds one value 16 v at a random
+    position; rotated, it becomes +-v on all 256 entries.  v is chosen so that
+    the FP32 product v * r (r the FP32 reciprocal of the FP32 scale) rounds to
+    exactly k + 1/2 while the exact product lies on the side of the odd
+    neighbour: rounding the FP32 product half to even gives the even code, and
+    rounding the exact product (a fused multiply-add style shortcut) gives the
+    odd one.  Returns the rows and the (row, block) list of the ties.
+    """
+    rng = np.random.default_rng(seed)
+    x = np.zeros((rows, nblocks * 256), np.float32)
+    ties = []
+    for m in range(rows):
+        A = np.float32(rng.uniform(1.0, 100.0))
+        x[m, 0] = np.float32(16) * A
+        s = np.float32(A / np.float32(127))
+        r = np.float32(np.float32(1) / s)
+        for b in range(1, nblocks):
+            for _ in range(64):
+                k = int(rng.integers(0, 126))
+                t = k + 0.5
+                v = np.float32(t / float(r))
+                for _ in range(64):
+                    exact = float(v) * float(r)          # exact in float64
+                    if np.float32(v * r) == np.float32(t) and (exact > t) == (k % 2 == 0) and exact != t:
+                        break
+                    v = np.nextafter(v, np.float32(np.inf) if exact < t else np.float32(0))
+                else:
+                    continue
+                break
+            else:
+                raise AssertionError("no tie found")
+            x[m, b * 256 + int(rng.integers(0, 256))] = np.float32(16) * v
+            ties.append((m, b))
+    return x, ties
+
+
+def test_quant_codes_round_the_fp32_product_half_to_even():
+    x, ties = _fp32_tie_rows(48, 12, seed=21)
+    K = x.shape[1]
+    rq, rs = oracle.quant_act(x, "fp32", K)
+    # the construction bites: every tie block holds even codes that the exact
+    # product would have rounded the other way
+    for m, b in ties[:50]:
+        blk = rq[m, b * 256:(b + 1) * 256].astype(np.int64)
+        assert np.all(blk % 2 == 0) and np.all(np.abs(blk) == abs(blk[0]))
+    for fmt in ("f16", "s8"):
+        q, s = gpu_quant_act(x, "fp32", K, fmt=fmt)
+        assert np.array_equal(codes_to_np(q, K), rq), fmt
+        assert np.array_equal(s.cpu().numpy(), rs), fmt
+
+
 # ---------------------------------------------------------------- kernel 1
 W_CASES = [
     ("tiny", synth.WORKLOADS["tiny"]),
