@@ -335,16 +335,50 @@ class E2EPipeline:
         return t0.elapsed_time(t1)
 
 
+def host_link_gbs(pipe: "E2EPipeline", reps: int = 3):
+    """Bandwidth of the host link alone on this machine, right before the timed
+    end-to-end run: the step's output copied to pinned host memory over the
+    pipeline's copy streams, and its activation input copied in (best of
+    `reps`).  The host link is shared with other work on the machine, so the
+    end-to-end figure is read against it."""
+    import torch
+    b = pipe.bufs[0]
+    parts = pipe.s_out_parts
+    rows = b["y"].shape[0]
+    step = -(-rows // len(parts))
+    best_out = best_in = 0.0
+    for _ in range(reps):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record()
+        for j, sp in enumerate(parts):
+            sp.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(sp):
+                b["hy"][j * step:(j + 1) * step].copy_(b["y"][j * step:(j + 1) * step], non_blocking=True)
+        for sp in parts:
+            torch.cuda.current_stream().wait_stream(sp)
+        t1.record()
+        t1.synchronize()
+        best_out = max(best_out, pipe.out_bytes / (t0.elapsed_time(t1) / 1e3) / 1e9)
+        t0.record()
+        b["x"].copy_(pipe.L.h_x, non_blocking=True)
+        t1.record()
+        t1.synchronize()
+        best_in = max(best_in, pipe.L.h_x.numel() * pipe.L.h_x.element_size() / (t0.elapsed_time(t1) / 1e3) / 1e9)
+    return {"d2h": best_out, "h2d": best_in}
+
+
 def time_e2e(layer: Layer, steps: int, warmup: int, world: int):
     import torch
     pipe = E2EPipeline(layer)
     pipe.run(warmup)
     torch.cuda.synchronize()
+    link = host_link_gbs(pipe)
     barrier(world)
     ms = pipe.run(steps)
     torch.cuda.synchronize()
     barrier(world)
-    return ms, pipe.in_bytes, pipe.out_bytes
+    return ms, pipe.in_bytes, pipe.out_bytes, link
 
 
 def time_ffn_block(dev, world, flush, warmup, steps=10):
@@ -615,11 +649,11 @@ def main():
     traffic = GEMM_TRAFFIC["bytes"] if GEMM_TRAFFIC["sha256_16"] == code_sha16(gemm_src) else None
 
     # end-to-end through the public API with host buffers
-    e2e_value = e2e_ms = None
+    e2e_value = e2e_ms = link = None
     h2d = layer.in_bytes
     d2h = layer.y.numel() * layer.y.element_size()
     if args.e2e_steps > 0:
-        e2e_ms, h2d, d2h = time_e2e(layer, args.e2e_steps, 3, world)
+        e2e_ms, h2d, d2h, link = time_e2e(layer, args.e2e_steps, 3, world)
         e2e_ms = reduce_max(e2e_ms, world)
         e2e_value = aggregate_tops(sz["ops"], args.e2e_steps, e2e_ms, world)
     if layer.cr.device_error() != 0:
@@ -707,7 +741,8 @@ def main():
         "hbm_peak_gbs": hbm,
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "pipelined": "streams: copy-in, kernels, copy-out split over 2 copy streams",
-                "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None},
+                "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None,
+                "host_link_gbs": link},
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],
         "cpu_baseline": cpu,

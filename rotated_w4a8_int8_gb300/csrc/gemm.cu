@@ -25,7 +25,11 @@
 // loads its own A tile and one half of the shared B tile, multicast into both
 // CTAs, so every SM pulls 32 KiB instead of 48 KiB from L2 per K step.  A
 // stage is refilled only after the MMAs of both CTAs have released it.
-// Clusters are persistent over a grouped tile order.  Warp 0: TMA producer.
+// When the number of M tiles is odd, the last M tile has no partner: its
+// tiles are done "solo", each CTA of a cluster taking its own N tile of that
+// M tile and loading the whole B tile without multicast, so the unpaired row
+// of tiles costs half a pass over N instead of a full one.  Clusters are
+// persistent over a grouped tile order.  Warp 0: TMA producer.
 // Warp 1: TMEM owner and MMA issuer.  Warps 2..9: epilogue, which applies
 // y = fp32(acc) * s_a * s_w (+ bias), stages 32-row x 64-byte boxes in
 // swizzled shared memory and writes them with TMA tensor stores (per-element
@@ -246,7 +250,8 @@ constexpr uint32_t kIdesc = (1u << 4)                         // D format: F32
 struct Params {
   int M, N, K_p;
   int num_m, num_n, k_steps;
-  int num_mp, num_pair_tiles;     // M-tile pairs (one per cluster) and pair tiles
+  int num_mp;          // M-tile pairs sharing B tiles (the last M tile is unpaired when num_m is odd)
+  int num_pair_tiles;  // work items of a cluster: num_mp * num_n shared items, then the solo items
   const float* a_scale;
   const float* w_scale;
   const float* bias;   // optional, [N]
@@ -267,6 +272,23 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   const int r = tile - g * per_group;
   mb = first_m + r % gsize;
   nb = r / gsize;
+}
+
+// Work item -> this CTA's (M tile, N tile).  Returns true for a shared item
+// (the pair's M tiles share one B tile, multicast), false for a solo item of
+// the unpaired last M tile (each CTA its own N tile; nb may be past the last
+// N tile for the second CTA, which then computes zeros and stores nothing).
+__device__ __forceinline__ bool work_coords(const Params& p, int item, int rank, int& mb, int& nb) {
+  const int shared_items = p.num_mp * p.num_n;
+  if (item < shared_items) {
+    int mp;
+    tile_coords(item, p.num_mp, p.num_n, mp, nb);
+    mb = mp * CLUSTER + rank;
+    return true;
+  }
+  mb = p.num_m - 1;
+  nb = (item - shared_items) * CLUSTER + rank;
+  return false;
 }
 
 // ------------------------------------------------------------------ epilogue stores
@@ -346,19 +368,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       bool ok = true;
       uint32_t issued_mask = 0, issued_phase = 0;   // last outstanding load per stage
       for (int tile = cluster_id; tile < p.num_pair_tiles && ok && !p.test_stall; tile += num_clusters) {
-        int mp, nb;
-        tile_coords(tile, p.num_mp, p.num_n, mp, nb);
-        const int mb = mp * CLUSTER + rank;
+        int mb, nb;
+        const bool shared_b = work_coords(p, tile, rank, mb, nb);
         for (int ks = 0; ks < k_steps; ++ks) {
           // the stage is free once the MMAs of BOTH CTAs have consumed it
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, ERR_WAIT_EMPTY, abort_flag)) { ok = false; break; }
           const uint32_t fb = full0 + 8 * stage;
-          // own A tile + both halves of B (ours and the peer's multicast)
+          // own A tile + both halves of B: ours and the peer's multicast, or
+          // (solo item) both halves of our own B tile
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           tma_load_2d(sa, &tmap_a, fb, ks * BK, mb * BM);
-          tma_load_2d_mc(sa + A_BYTES + rank * B_HALF_BYTES, &tmap_b, fb, ks * BK,
-                         nb * BN + rank * (BN / CLUSTER), kPeers);
+          if (shared_b) {
+            tma_load_2d_mc(sa + A_BYTES + rank * B_HALF_BYTES, &tmap_b, fb, ks * BK,
+                           nb * BN + rank * (BN / CLUSTER), kPeers);
+          } else {
+#pragma unroll
+            for (int h = 0; h < CLUSTER; ++h)
+              tma_load_2d(sa + A_BYTES + h * B_HALF_BYTES, &tmap_b, fb, ks * BK, nb * BN + h * (BN / CLUSTER));
+          }
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -430,9 +458,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint32_t boxes = 0;                       // output boxes staged by this warp so far
     bool ok = true;
     for (int tile = cluster_id; tile < p.num_pair_tiles && ok; tile += num_clusters) {
-      int mp, nb;
-      tile_coords(tile, p.num_mp, p.num_n, mp, nb);
-      const int mb = mp * CLUSTER + rank;
+      int mb, nb;
+      work_coords(p, tile, rank, mb, nb);
       int32_t acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0;
@@ -694,8 +721,8 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.K_p = K_p;
   p.num_m = (M + BM - 1) / BM;
   p.num_n = (N + BN - 1) / BN;
-  p.num_mp = (p.num_m + CLUSTER - 1) / CLUSTER;
-  p.num_pair_tiles = p.num_mp * p.num_n;
+  p.num_mp = p.num_m / CLUSTER;
+  p.num_pair_tiles = p.num_mp * p.num_n + (p.num_m % CLUSTER ? (p.num_n + CLUSTER - 1) / CLUSTER : 0);
   p.k_steps = K_p / BK;
   p.a_scale = a_scale;
   p.w_scale = w_scale;

@@ -189,7 +189,7 @@ def test_prepare_weight_ignores_serialised_padding():
 
 # ---------------------------------------------------------------- kernel 3
 GEMM_SHAPES = [(128, 256, 256), (300, 520, 1280), (1, 1, 256), (129, 257, 768), (513, 300, 5376),
-               (64, 1000, 512), (130, 260, 65536)]
+               (64, 1000, 512), (130, 260, 65536), (2100, 1300, 512)]
 
 
 @pytest.mark.parametrize("M,N,Kp", GEMM_SHAPES)
