@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from the ncu capture
 # summarised in profiles/gemm_tcgen05_qkv.md; valid only while code_sha16(gemm.cu) equals this
 # (the hash ignores comments; otherwise the bench line reports traffic as null).
-GEMM_TRAFFIC = {"sha256_16": "62d8bf76ca27beb5", "bytes": 2759375104 + 875473664}
+GEMM_TRAFFIC = {"sha256_16": "8d8c2a70bcebb0bc", "bytes": 3078212352 + 894041088}
 
 
 def code_sha16(path: str) -> str:

@@ -306,7 +306,9 @@ template <> __device__ __forceinline__ float to_out<CONVROT_FP32>(float y) { ret
 
 // OUT = CONVROT_BF16 / FP16 / FP32, or -1 for raw int32 accumulators.
 // BIAS: p.bias is non-null and added in the epilogue.
-template <int OUT, bool BIAS>
+// TMA_OUT: staged output boxes go out by TMA tensor stores (output base and
+// pitch 16-byte aligned); otherwise the warp writes them with element stores.
+template <int OUT, bool BIAS, bool TMA_OUT>
 __global__ void __launch_bounds__(THREADS, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_out, const Params p) {
@@ -503,7 +505,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         using T = typename OutT<OUT>::T;
         constexpr int VEC = 16 / sizeof(T);           // outputs per 16-byte chunk
         const float sa = (m < p.M) ? __ldg(p.a_scale + m) : 0.f;
-        if (p.out_tma) {
+        {
+          // staged 32-row boxes, written by a TMA tensor store, or (output
+          // base or pitch not 16-byte aligned) by the warp with element
+          // stores that walk each row: consecutive lanes, consecutive columns
           constexpr int CPB = OUT_BOX_BYTES / sizeof(T);   // columns per box
           uint8_t* wstage = staging + ew * 2 * OUT_BOX;
 #pragma unroll
@@ -549,37 +554,30 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
               // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
               *reinterpret_cast<uint4*>(rowp + ((c ^ ((lane >> 1) & 3)) << 4)) = pk.u;
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            // boxes wholly outside the matrix (M or N tail) are not stored
-            if (lane == 0 && m_base < p.M && n0 + b * CPB < p.N) {
-              tma_store_2d(&tmap_out, smem_u32(wstage + buf * OUT_BOX), n0 + b * CPB, m_base);
-              bulk_commit();
-            }
-          }
-        } else if (m < p.M) {
-          T* orow = static_cast<T*>(p.out) + static_cast<int64_t>(m) * p.ld_out;
-#pragma unroll
-          for (int j0 = 0; j0 < 128; j0 += VEC) {
-            const int n = n0 + j0;
-            if (p.out_vec && n + VEC <= p.N) {
-              union { T v[VEC]; uint4 u; } pk;
-#pragma unroll
-              for (int j = 0; j < VEC; ++j) {
-                float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa), __ldg(p.w_scale + n + j));
-                if constexpr (BIAS) y = __fadd_rn(y, __ldg(p.bias + n + j));
-                pk.v[j] = to_out<OUT>(y);
+            if constexpr (TMA_OUT) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              // boxes wholly outside the matrix (M or N tail) are not stored
+              if (lane == 0 && m_base < p.M && n0 + b * CPB < p.N) {
+                tma_store_2d(&tmap_out, smem_u32(wstage + buf * OUT_BOX), n0 + b * CPB, m_base);
+                bulk_commit();
               }
-              *reinterpret_cast<uint4*>(orow + n) = pk.u;
             } else {
-#pragma unroll
-              for (int j = 0; j < VEC; ++j) {
-                if (n + j < p.N) {
-                  float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + j]), sa), __ldg(p.w_scale + n + j));
-                  if constexpr (BIAS) y = __fadd_rn(y, __ldg(p.bias + n + j));
-                  orow[n + j] = to_out<OUT>(y);
+              __syncwarp();
+              const uint8_t* box = wstage + buf * OUT_BOX;
+#pragma unroll 4
+              for (int it = 0; it < CPB; ++it) {
+                const int idx = it * 32 + lane;              // element of the 32 x CPB box, row-major
+                const int r = idx / CPB, col = idx % CPB;
+                const int bo = col * static_cast<int>(sizeof(T));
+                const int mr = m_base + r, n = n0 + b * CPB + col;
+                if (mr < p.M && n < p.N) {
+                  const T v = *reinterpret_cast<const T*>(box + r * OUT_BOX_BYTES +
+                                                          ((((bo >> 4) ^ ((r >> 1) & 3))) << 4) + (bo & 15));
+                  static_cast<T*>(p.out)[static_cast<int64_t>(mr) * p.ld_out + n] = v;
                 }
               }
+              __syncwarp();                                  // box read before its buffer is refilled
             }
           }
         }
@@ -655,7 +653,7 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int
 
 // Persistent grid: as many clusters as can be resident at once (one CTA per
 // SM), never more than there are pair tiles.
-template <int OUT, bool BIAS>
+template <int OUT, bool BIAS, bool TMA_OUT>
 static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                           const Params& p, cudaStream_t st) {
   static int max_clusters_by_dev[64] = {0};   // resident clusters, per device and instantiation
@@ -678,14 +676,14 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT, BIAS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<OUT, BIAS, TMA_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          SMEM_BYTES);
     if (e != cudaSuccess) return e;
     int sms = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     cfg.gridDim = dim3(sms / CLUSTER * CLUSTER);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<OUT, BIAS>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_kernel<OUT, BIAS, TMA_OUT>, &cfg);
     if (e != cudaSuccess || n <= 0) {
       (void)cudaGetLastError();
       n = sms / CLUSTER;
@@ -694,7 +692,14 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   }
   const int clusters = p.num_pair_tiles < max_clusters ? p.num_pair_tiles : max_clusters;
   cfg.gridDim = dim3(clusters * CLUSTER);
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<OUT, BIAS>, ma, mb, mo, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<OUT, BIAS, TMA_OUT>, ma, mb, mo, p);
+}
+
+template <int OUT>
+static cudaError_t launch_out(bool bias, bool tma, const CUtensorMap& ma, const CUtensorMap& mb,
+                              const CUtensorMap& mo, const Params& p, cudaStream_t st) {
+  if (bias) return tma ? launch<OUT, true, true>(ma, mb, mo, p, st) : launch<OUT, true, false>(ma, mb, mo, p, st);
+  return tma ? launch<OUT, false, true>(ma, mb, mo, p, st) : launch<OUT, false, false>(ma, mb, mo, p, st);
 }
 
 static int validate_operands(const void* a_q, int64_t ld_aq, const void* w_q, int64_t ld_wq, int M,
@@ -739,10 +744,10 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   cudaError_t e;
   const bool b = bias != nullptr;
   switch (out_kind) {
-    case CONVROT_BF16: e = b ? launch<CONVROT_BF16, true>(ma, mb, mo, p, stream) : launch<CONVROT_BF16, false>(ma, mb, mo, p, stream); break;
-    case CONVROT_FP16: e = b ? launch<CONVROT_FP16, true>(ma, mb, mo, p, stream) : launch<CONVROT_FP16, false>(ma, mb, mo, p, stream); break;
-    case CONVROT_FP32: e = b ? launch<CONVROT_FP32, true>(ma, mb, mo, p, stream) : launch<CONVROT_FP32, false>(ma, mb, mo, p, stream); break;
-    default: e = launch<-1, false>(ma, mb, mo, p, stream); break;
+    case CONVROT_BF16: e = launch_out<CONVROT_BF16>(b, p.out_tma != 0, ma, mb, mo, p, stream); break;
+    case CONVROT_FP16: e = launch_out<CONVROT_FP16>(b, p.out_tma != 0, ma, mb, mo, p, stream); break;
+    case CONVROT_FP32: e = launch_out<CONVROT_FP32>(b, p.out_tma != 0, ma, mb, mo, p, stream); break;
+    default: e = launch<-1, false, false>(ma, mb, mo, p, stream); break;
   }
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("GEMM launch", e);
 }

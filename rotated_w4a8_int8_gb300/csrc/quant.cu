@@ -256,6 +256,25 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
   }
 }
 
+// L2 prefetch of a later row.  Each CTA reads its row once, at its start,
+// and then computes with nothing in flight; the loads of the CTAs resident
+// on an SM alone do not keep HBM busy.  So every CTA also prefetches into
+// L2 the row that a CTA about kPfBytes of input later will read (one
+// prefetch.global.L2 per 128-byte line, spread over the threads), and that
+// CTA then finds its row in L2.  The distance is kPfBytes / row bytes rows,
+// between 32 and 512: long enough to cover the HBM latency, short enough
+// that the prefetched rows stay far below the L2 size.
+constexpr size_t kPfBytes = size_t(8) << 20;
+
+__device__ __forceinline__ int prefetch_distance(size_t row_bytes) {
+  return static_cast<int>(min(size_t(512), max(size_t(32), kPfBytes / row_bytes)));
+}
+
+__device__ __forceinline__ void l2_prefetch(const char* p, size_t bytes) {
+  for (size_t off = static_cast<size_t>(threadIdx.x) * 128; off < bytes; off += static_cast<size_t>(blockDim.x) * 128)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
+}
+
 // Kernel 2: one CTA per activation row, or (SPLIT == 2) a cluster of two
 // CTAs per row, each owning half of the row's blocks.
 template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE, int SPLIT>
@@ -274,6 +293,15 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nbl
   ActRaw<DT, SWIGLU, NBMAX> cur;
   load_act_row<DT, SWIGLU, NBMAX, VEC>(static_cast<const char*>(x) + static_cast<size_t>(row) * ld_x * esize,
                                        K, blk0, nloc, S, slot, lane8, cur);
+  {
+    // this CTA's share (its part of the row) of a later row
+    const size_t rb = static_cast<size_t>(SWIGLU ? 2 * K : K) * esize;
+    const int later = row + prefetch_distance(rb);
+    if (later < M) {
+      const size_t share = (rb + SPLIT - 1) / SPLIT, b0 = part * share, b1 = min(rb, b0 + share);
+      l2_prefetch(static_cast<const char*>(x) + static_cast<size_t>(later) * ld_x * esize + b0, b1 - b0);
+    }
+  }
   act_row<DT, SWIGLU, NBMAX, PRESCALE, SPLIT>(cur, row, K, blk0, nloc, S, slot, lane8, smem + slot * kSlotBytes,
                                               red, xred, pre_scale, q, f16_codes, ld_q, scale);
   if constexpr (SPLIT == 2) cluster_exit_wait();
@@ -378,6 +406,14 @@ prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
   const int blk0 = part * nbl, nloc = min(nbl, nblocks - blk0);
   WRaw<NBMAX> r0;
   load_weight_row<NBMAX, W16>(w_fp4, w_sf, row, K, K_s, blk0, nloc, S, slot, lane8, r0);
+  {
+    // short weight rows (under 4 KiB packed) gain nothing measurable from it
+    const int later = row + prefetch_distance((K_s >> 1) + (K_s >> 4));
+    if (later < N && part == 0 && (K_s >> 1) >= 4096) {
+      l2_prefetch(reinterpret_cast<const char*>(w_fp4) + static_cast<size_t>(later) * (K_s >> 1), K_s >> 1);
+      l2_prefetch(reinterpret_cast<const char*>(w_sf) + static_cast<size_t>(later) * (K_s >> 4), K_s >> 4);
+    }
+  }
   weight_row<NBMAX, SPLIT>(r0, row, K, blk0, nloc, S, slot, lane8, t16, smem + slot * kSlotBytes, red, xred, q,
                            f16_codes, ld_q, scale);
   if constexpr (SPLIT == 2) cluster_exit_wait();

@@ -242,7 +242,10 @@ def test_gemm_dequant_given_identical_operands(out_dtype):
     assert np.all(np.abs(got - ref) <= ulp * 2.0 ** np.floor(np.log2(mag)) * 1.0001)
 
 
-def test_gemm_output_pitch_guard_and_unaligned_base():
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp16", "fp32"])
+def test_gemm_output_pitch_guard_and_unaligned_base(out_dtype):
+    # an output view whose base and pitch are not 16-byte aligned takes the
+    # per-element store path of the epilogue; nothing around it may change
     rng = np.random.default_rng(22)
     M, N, Kp = 140, 270, 512
     qa = rng.integers(-127, 128, (M, Kp)).astype(np.int8)
@@ -250,13 +253,14 @@ def test_gemm_output_pitch_guard_and_unaligned_base():
     sa = np.full(M, 1e-3, np.float32)
     sw = np.full(N, 1e-3, np.float32)
     import rotated_w4a8_int8_gb300 as cr
-    big = torch.full((M + 1, N + 9), -7.0, dtype=torch.bfloat16, device=DEV)
-    view = big[:M, 1:N + 1]               # base 2 bytes past a 16-byte boundary
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}[out_dtype]
+    big = torch.full((M + 1, N + 9), -7.0, dtype=tdt, device=DEV)
+    view = big[:M, 1:N + 1]               # base one element past a 16-byte boundary
     cr.gemm(f16_codes_from_np(qa), torch.from_numpy(sa).to(DEV), f16_codes_from_np(qw),
             torch.from_numpy(sw).to(DEV), view, K_p=Kp)
     b = big.float().cpu().numpy()
     assert np.all(b[:, 0] == -7) and np.all(b[:, N + 1:] == -7) and np.all(b[M] == -7)
-    ref = oracle.dequantize(oracle.int_gemm(qa, qw), sa, sw, "bf16")
+    ref = oracle.dequantize(oracle.int_gemm(qa, qw), sa, sw, out_dtype)
     assert_output_match(b[:M, 1:N + 1], ref)
 
 
