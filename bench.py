@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from the ncu capture
 # summarised in profiles/gemm_tcgen05_qkv.md; valid only while code_sha16(gemm.cu) equals this
 # (the hash ignores comments; otherwise the bench line reports traffic as null).
-GEMM_TRAFFIC = {"sha256_16": "8d8c2a70bcebb0bc", "bytes": 3078212352 + 894041088}
+GEMM_TRAFFIC = {"sha256_16": "a160da7c3a25735b", "bytes": 2979521792 + 912784640}
 
 
 def code_sha16(path: str) -> str:
@@ -336,20 +336,22 @@ class E2EPipeline:
 
 
 def host_link_gbs(pipe: "E2EPipeline", reps: int = 3):
-    """Bandwidth of the host link alone on this machine, right before the timed
-    end-to-end run: the step's output copied to pinned host memory over the
-    pipeline's copy streams, and its activation input copied in (best of
-    `reps`).  The host link is shared with other work on the machine, so the
-    end-to-end figure is read against it."""
+    """The host link on this machine, right before the timed end-to-end run (best
+    of `reps`): the step's output copied to pinned host memory over the
+    pipeline's copy streams, alone ("d2h") and while two layers run on the
+    pipeline's kernel stream ("d2h_beside_kernels", with the layers' own
+    time beside it); the activation input copied in alone ("h2d").  The host
+    link is shared with other work on the machine, so the end-to-end figure
+    is read against these."""
     import torch
     b = pipe.bufs[0]
     parts = pipe.s_out_parts
     rows = b["y"].shape[0]
     step = -(-rows // len(parts))
-    best_out = best_in = 0.0
-    for _ in range(reps):
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def copy_out():
+        t0, t1 = ev(), ev()
         t0.record()
         for j, sp in enumerate(parts):
             sp.wait_stream(torch.cuda.current_stream())
@@ -358,14 +360,36 @@ def host_link_gbs(pipe: "E2EPipeline", reps: int = 3):
         for sp in parts:
             torch.cuda.current_stream().wait_stream(sp)
         t1.record()
+        return t0, t1
+
+    out = {"d2h": 0.0, "h2d": 0.0, "d2h_beside_kernels": 0.0, "kernels_beside_d2h_ms": None}
+    L = pipe.L
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        t0, t1 = copy_out()
         t1.synchronize()
-        best_out = max(best_out, pipe.out_bytes / (t0.elapsed_time(t1) / 1e3) / 1e9)
+        out["d2h"] = max(out["d2h"], pipe.out_bytes / (t0.elapsed_time(t1) / 1e3) / 1e9)
+        t0, t1 = ev(), ev()
         t0.record()
-        b["x"].copy_(pipe.L.h_x, non_blocking=True)
+        b["x"].copy_(L.h_x, non_blocking=True)
         t1.record()
         t1.synchronize()
-        best_in = max(best_in, pipe.L.h_x.numel() * pipe.L.h_x.element_size() / (t0.elapsed_time(t1) / 1e3) / 1e9)
-    return {"d2h": best_out, "h2d": best_in}
+        out["h2d"] = max(out["h2d"], L.h_x.numel() * L.h_x.element_size() / (t0.elapsed_time(t1) / 1e3) / 1e9)
+        # the copy beside two layers on the kernel stream
+        torch.cuda.synchronize()
+        k0, k1 = ev(), ev()
+        pipe.s_run.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(pipe.s_run):
+            k0.record()
+            for _ in range(2):
+                L.step()
+            k1.record()
+        t0, t1 = copy_out()
+        torch.cuda.synchronize()
+        out["d2h_beside_kernels"] = max(out["d2h_beside_kernels"],
+                                        pipe.out_bytes / (t0.elapsed_time(t1) / 1e3) / 1e9)
+        out["kernels_beside_d2h_ms"] = k0.elapsed_time(k1) / 2
+    return out
 
 
 def time_e2e(layer: Layer, steps: int, warmup: int, world: int):

@@ -251,12 +251,12 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
     const int li = slot + S * i;
     if (slot < S && li < nloc) {
       scale_cols(c[i], mult);
-      store_codes(qrow, f16_codes, blk0 + li, lane8, c[i]);
+      store_codes<SWIGLU>(qrow, f16_codes, blk0 + li, lane8, c[i]);
     }
   }
 }
 
-// L2 prefetch of a later row.  Each CTA reads its row once, at its start,
+// L2 prefetch of a later activation row.  Each CTA reads its row once, at its start,
 // and then computes with nothing in flight; the loads of the CTAs resident
 // on an SM alone do not keep HBM busy.  So every CTA also prefetches into
 // L2 the row that a CTA about kPfBytes of input later will read (one
@@ -384,7 +384,7 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
     const int li = slot + S * i;
     if (slot < S && li < nloc) {
       scale_cols(c[i], rq.r);
-      store_codes(qrow, f16_codes, blk0 + li, lane8, c[i]);
+      store_codes<false>(qrow, f16_codes, blk0 + li, lane8, c[i]);
     }
   }
 }
@@ -406,14 +406,6 @@ prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
   const int blk0 = part * nbl, nloc = min(nbl, nblocks - blk0);
   WRaw<NBMAX> r0;
   load_weight_row<NBMAX, W16>(w_fp4, w_sf, row, K, K_s, blk0, nloc, S, slot, lane8, r0);
-  {
-    // short weight rows (under 4 KiB packed) gain nothing measurable from it
-    const int later = row + prefetch_distance((K_s >> 1) + (K_s >> 4));
-    if (later < N && part == 0 && (K_s >> 1) >= 4096) {
-      l2_prefetch(reinterpret_cast<const char*>(w_fp4) + static_cast<size_t>(later) * (K_s >> 1), K_s >> 1);
-      l2_prefetch(reinterpret_cast<const char*>(w_sf) + static_cast<size_t>(later) * (K_s >> 4), K_s >> 4);
-    }
-  }
   weight_row<NBMAX, SPLIT>(r0, row, K, blk0, nloc, S, slot, lane8, t16, smem + slot * kSlotBytes, red, xred, q,
                            f16_codes, ld_q, scale);
   if constexpr (SPLIT == 2) cluster_exit_wait();

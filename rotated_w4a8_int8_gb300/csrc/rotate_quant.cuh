@@ -201,25 +201,41 @@ struct RowQuant {
   }
 };
 
-// Round half to even, for |v| < 2^22.  Adding 1.5 * 2^23 moves v to where
-// the FP32 spacing is 1, so the (nearest-even) add itself rounds v to an
-// integer, and subtracting the constant back is exact.  The bit pattern of
-// the sum is 0x4B400000 + code, so its low byte is the two's-complement S8
-// code.  __fadd_rn / __fsub_rn are never contracted into a multiply-add with
-// the product before them (that would round the exact product instead of the
-// FP32 one).  The adds run on the FP32 pipe; a cvt.rni conversion goes to a
-// pipe with an eighth of its rate (16 per clock per SM, measured), which the
-// SwiGLU prologue's exponentials and reciprocals already load.
+// Round half to even of the FP32 product, two equivalent ways (bit-identical
+// codes; the kernel picks the one whose pipe has room):
+//  - cvt.rni.f32.f32: one instruction, on a conversion pipe that does 16
+//    results per clock per SM (measured), an eighth of the FP32 add rate;
+//  - adding 1.5 * 2^23 (|v| < 2^22): v lands where the FP32 spacing is 1, so
+//    the nearest-even add itself rounds v to an integer, and subtracting the
+//    constant back is exact; the bit pattern of the sum is 0x4B400000 + code,
+//    so its low byte is the two's-complement S8 code.  __fadd_rn / __fsub_rn
+//    are never contracted into a multiply-add with the product before them
+//    (that would round the exact product instead of the FP32 one).
+// The weight and plain activation kernels are bound by instruction issue and
+// take cvt.rni (fewer instructions); the SwiGLU kernel's exponentials and
+// reciprocals already load the conversion pipe, so it takes the adds.
 constexpr float kRoundMagic = 12582912.0f;
 
-__device__ __forceinline__ float round_magic(float v) { return __fadd_rn(v, kRoundMagic); }
+template <bool MAGIC>
+__device__ __forceinline__ float rint_f(float v) {
+  if constexpr (MAGIC) {
+    return __fsub_rn(__fadd_rn(v, kRoundMagic), kRoundMagic);
+  } else {
+    float d;
+    asm("cvt.rni.f32.f32 %0, %1;" : "=f"(d) : "f"(v));
+    return d;
+  }
+}
 
-__device__ __forceinline__ float rint_f(float v) { return __fsub_rn(round_magic(v), kRoundMagic); }
-
-__device__ __forceinline__ uint32_t code_byte(float v) { return __float_as_uint(round_magic(v)) & 0xffu; }
+template <bool MAGIC>
+__device__ __forceinline__ uint32_t code_byte(float v) {
+  if constexpr (MAGIC) return __float_as_uint(__fadd_rn(v, kRoundMagic)) & 0xffu;
+  else return static_cast<uint32_t>(__float2int_rn(v)) & 0xffu;
+}
 
 // Writes the codes of one block: values (already multiplied by r, so only
 // the rounding is left) for rows 2p, 2p+1 and columns 2q, 2q+1.
+template <bool MAGIC>
 __device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk, int lane8,
                                             const BlockCols& c) {
   const int col = blk * kBlock + 2 * lane8;
@@ -227,15 +243,15 @@ __device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk
     __half2* q = reinterpret_cast<__half2*>(static_cast<__half*>(q_row) + col);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-      q[(32 * p) / 2] = __floats2half2_rn(rint_f(c.U[p].x), rint_f(c.V[p].x));        // row 2p
-      q[(32 * p + 16) / 2] = __floats2half2_rn(rint_f(c.U[p].y), rint_f(c.V[p].y));   // row 2p+1
+      q[(32 * p) / 2] = __floats2half2_rn(rint_f<MAGIC>(c.U[p].x), rint_f<MAGIC>(c.V[p].x));        // row 2p
+      q[(32 * p + 16) / 2] = __floats2half2_rn(rint_f<MAGIC>(c.U[p].y), rint_f<MAGIC>(c.V[p].y));   // row 2p+1
     }
   } else {
     uint16_t* q = reinterpret_cast<uint16_t*>(static_cast<int8_t*>(q_row) + col);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-      q[(32 * p) / 2] = static_cast<uint16_t>(code_byte(c.U[p].x) | (code_byte(c.V[p].x) << 8));
-      q[(32 * p + 16) / 2] = static_cast<uint16_t>(code_byte(c.U[p].y) | (code_byte(c.V[p].y) << 8));
+      q[(32 * p) / 2] = static_cast<uint16_t>(code_byte<MAGIC>(c.U[p].x) | (code_byte<MAGIC>(c.V[p].x) << 8));
+      q[(32 * p + 16) / 2] = static_cast<uint16_t>(code_byte<MAGIC>(c.U[p].y) | (code_byte<MAGIC>(c.V[p].y) << 8));
     }
   }
 }

@@ -152,6 +152,23 @@ def test_quant_codes_round_the_fp32_product_half_to_even():
         assert np.array_equal(s.cpu().numpy(), rs), fmt
 
 
+def test_swiglu_quant_codes_round_the_fp32_product_half_to_even():
+    # the SwiGLU kernel rounds through FP32 adds, the others through cvt.rni:
+    # the same tie rows, fed through the SwiGLU prologue.  A gate of 128 makes
+    # exp(-g) underflow to 0 in FP32 and FP64 alike, so h = 128 v exactly and
+    # the value half carries the tie rows divided by 128 (a power of two).
+    ties, _ = _fp32_tie_rows(32, 12, seed=24)
+    K = ties.shape[1]
+    x = np.concatenate([np.full_like(ties, 128.0), ties / np.float32(128.0)], axis=1).astype(np.float32)
+    rq, rs = oracle.quant_act(x, "fp32", K, True)
+    rq0, rs0 = oracle.quant_act(ties, "fp32", K)
+    assert np.array_equal(rq, rq0) and np.array_equal(rs, rs0)
+    for fmt in ("f16", "s8"):
+        q, s = gpu_quant_act(x, "fp32", K, swiglu=True, fmt=fmt)
+        assert np.array_equal(codes_to_np(q, K), rq), fmt
+        assert np.array_equal(s.cpu().numpy(), rs), fmt
+
+
 # ---------------------------------------------------------------- kernel 1
 W_CASES = [
     ("tiny", synth.WORKLOADS["tiny"]),
@@ -185,6 +202,42 @@ def test_prepare_weight_ignores_serialised_padding():
     qa, sa = gpu_prepare_weight(packed, scales, t, wl.K)
     qb, sb = gpu_prepare_weight(dirty, scales, t, wl.K)
     assert torch.equal(qa, qb) and torch.equal(sa, sb)
+
+
+GUARD_CASES = [("qkv_rows", small("qkv", 40, 24)), ("wide_rows", small("wide_k", 12, 8)),
+               ("ragged_rows", small("ragged", 21, 9)),
+               ("max_kp", synth.Workload("maxkpg", 3, 65536, 3, "bf16", "bf16", False, 0.01, 20.0, 23))]
+
+
+@pytest.mark.parametrize("case,wl", GUARD_CASES, ids=[c[0] for c in GUARD_CASES])
+@pytest.mark.parametrize("fmt", ["f16", "s8"])
+def test_quant_kernels_write_nothing_outside_their_outputs(case, wl, fmt):
+    # codes and scales sit inside poisoned buffers: extra columns past K_p (a
+    # wider pitch), a row after the last and a scale after the last must keep
+    # the poison; inside, the results equal those of the plain layout
+    import rotated_w4a8_int8_gb300 as cr
+    Kp = oracle.padded_k(wl.K)
+    dt = torch.float16 if fmt == "f16" else torch.int8
+    poison = 77
+    x = synth.make_activations(wl)
+    packed, scales, t = synth.make_nvfp4_weight(wl)
+    for rows, run, ref in (
+            (wl.M, lambda q, s: cr.quant_act(storage_to_dev(x, wl.x_dtype), wl.K, q, s),
+             lambda: gpu_quant_act(x, wl.x_dtype, wl.K, fmt=fmt)),
+            (wl.N, lambda q, s: cr.prepare_weight(torch.from_numpy(packed).to(DEV), torch.from_numpy(scales).to(DEV),
+                                                  torch.tensor([float(t)], dtype=torch.float32, device=DEV),
+                                                  wl.K, q, s),
+             lambda: gpu_prepare_weight(packed, scales, t, wl.K, fmt=fmt))):
+        big = torch.full((rows + 1, Kp + 64), poison, dtype=dt, device=DEV)
+        sbig = torch.full((rows + 1,), float(poison), dtype=torch.float32, device=DEV)
+        run(big[:rows], sbig[:rows])
+        torch.cuda.synchronize()
+        b = big.to(torch.int32).cpu().numpy()
+        assert np.all(b[:, Kp:] == poison) and np.all(b[rows] == poison)
+        assert float(sbig[rows]) == float(poison)
+        q, s = ref()
+        assert np.array_equal(b[:rows, :Kp], codes_to_np(q, Kp))
+        assert torch.equal(sbig[:rows], s)
 
 
 # ---------------------------------------------------------------- kernel 3
