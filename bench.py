@@ -362,7 +362,8 @@ def host_link_gbs(pipe: "E2EPipeline", reps: int = 3):
         t1.record()
         return t0, t1
 
-    out = {"d2h": 0.0, "h2d": 0.0, "d2h_beside_kernels": 0.0, "kernels_beside_d2h_ms": None}
+    out = {"d2h": 0.0, "h2d": 0.0, "d2h_beside_kernels": 0.0, "kernels_beside_d2h_ms": None,
+           "d2h_beside_h2d": 0.0}
     L = pipe.L
     for _ in range(reps):
         torch.cuda.synchronize()
@@ -389,6 +390,13 @@ def host_link_gbs(pipe: "E2EPipeline", reps: int = 3):
         out["d2h_beside_kernels"] = max(out["d2h_beside_kernels"],
                                         pipe.out_bytes / (t0.elapsed_time(t1) / 1e3) / 1e9)
         out["kernels_beside_d2h_ms"] = k0.elapsed_time(k1) / 2
+        # the copy beside the next step's input copy
+        pipe.s_in.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(pipe.s_in):
+            pipe.bufs[1]["x"].copy_(L.h_x, non_blocking=True)
+        t0, t1 = copy_out()
+        torch.cuda.synchronize()
+        out["d2h_beside_h2d"] = max(out["d2h_beside_h2d"], pipe.out_bytes / (t0.elapsed_time(t1) / 1e3) / 1e9)
     return out
 
 
