@@ -240,9 +240,8 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
     if (active) amax = absmax_cols(amax, c[i]);
   }
   // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
-  float zmax = cta_absmax(amax, red);
-  if constexpr (SPLIT == 2) zmax = cluster_pair_absmax(zmax, xred);
-  const RowQuant rq(zmax * 0.0625f);
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, red, 0.0625f)
+                                 : RowQuant(cluster_pair_absmax(cta_absmax(amax, red), xred) * 0.0625f);
   if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
   const float mult = rq.r * 0.0625f;           // fp32(z * (r / 16)) == fp32((z / 16) * r)
@@ -263,11 +262,14 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
 // prefetch.global.L2 per 128-byte line, spread over the threads), and that
 // CTA then finds its row in L2.  The distance is kPfBytes / row bytes rows,
 // between 32 and 512: long enough to cover the HBM latency, short enough
-// that the prefetched rows stay far below the L2 size.
+// that the prefetched rows stay far below the L2 size.  It is computed on
+// the host: a 64-bit division in every thread would cost more than the
+// prefetch itself.
 constexpr size_t kPfBytes = size_t(8) << 20;
 
-__device__ __forceinline__ int prefetch_distance(size_t row_bytes) {
-  return static_cast<int>(min(size_t(512), max(size_t(32), kPfBytes / row_bytes)));
+static int prefetch_distance(size_t row_bytes) {
+  const size_t d = kPfBytes / (row_bytes > 0 ? row_bytes : 1);
+  return static_cast<int>(d < 32 ? 32 : d > 512 ? 512 : d);
 }
 
 __device__ __forceinline__ void l2_prefetch(const char* p, size_t bytes) {
@@ -279,7 +281,7 @@ __device__ __forceinline__ void l2_prefetch(const char* p, size_t bytes) {
 // CTAs per row, each owning half of the row's blocks.
 template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE, int SPLIT>
 __global__ void __launch_bounds__(kMaxThreads)
-quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S,
+quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S, int pf_dist,
                  const float* __restrict__ pre_scale, void* __restrict__ q, int f16_codes, int64_t ld_q,
                  float* __restrict__ scale) {
   extern __shared__ __align__(16) char smem[];
@@ -296,7 +298,7 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nbl
   {
     // this CTA's share (its part of the row) of a later row
     const size_t rb = static_cast<size_t>(SWIGLU ? 2 * K : K) * esize;
-    const int later = row + prefetch_distance(rb);
+    const int later = row + pf_dist;
     if (later < M) {
       const size_t share = (rb + SPLIT - 1) / SPLIT, b0 = part * share, b1 = min(rb, b0 + share);
       l2_prefetch(static_cast<const char*>(x) + static_cast<size_t>(later) * ld_x * esize + b0, b1 - b0);
@@ -374,9 +376,8 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
       amax = absmax_cols(amax, c[i]);
     }
   }
-  float wmax = cta_absmax(amax, red);
-  if constexpr (SPLIT == 2) wmax = cluster_pair_absmax(wmax, xred);
-  const RowQuant rq(wmax);
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, red, 1.0f)
+                                 : RowQuant(cluster_pair_absmax(cta_absmax(amax, red), xred));
   if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
 #pragma unroll
@@ -476,7 +477,8 @@ static cudaError_t launch_act_cfg(const RowGeometry& g, int M, const void* x, in
                                   const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
   auto k = ps ? quant_act_kernel<DT, SWIGLU, NB, VEC, true, SPLIT>
               : quant_act_kernel<DT, SWIGLU, NB, VEC, false, SPLIT>;
-  return launch_rows(k, g, M, st, x, ld_x, M, K, g.nblocks, g.S, ps, q, f16, ld_q, scale);
+  const int pf = prefetch_distance(static_cast<size_t>(SWIGLU ? 2 * K : K) * (DT == DT_FP32 ? 4 : 2));
+  return launch_rows(k, g, M, st, x, ld_x, M, K, g.nblocks, g.S, pf, ps, q, f16, ld_q, scale);
 }
 
 template <int DT, bool SWIGLU, int VEC>

@@ -189,17 +189,41 @@ __device__ __forceinline__ void cluster_exit_wait() {
 // s = 0 and all-zero codes.
 struct RowQuant {
   float s, r;
-  bool degenerate;
   __device__ __forceinline__ explicit RowQuant(float amax) {
     s = __fdiv_rn(amax, 127.0f);
     r = __frcp_rn(s);
-    degenerate = (s == 0.0f) || isinf(r);
-    if (degenerate) {
+    if ((s == 0.0f) || isinf(r)) {    // degenerate row
       s = 0.0f;
       r = 0.0f;
     }
   }
+  __device__ __forceinline__ RowQuant(float s_, float r_) : s(s_), r(r_) {}
 };
+
+// Row absmax and quantiser of a row held by one CTA, set up once: warp 0
+// reduces the per-warp maxima and computes s and r from amax * pre; every
+// thread reads them after a second barrier.  Cheaper than every warp
+// reducing the maxima and computing the division and the reciprocal itself.
+// `red` holds one float per warp plus s and r at [16], [17].
+__device__ __forceinline__ RowQuant cta_rowquant(float local, float* red, float pre) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  if (lane == 0) red[warp] = local;
+  __syncthreads();
+  if (warp == 0) {
+    float m = lane < nwarps ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const RowQuant q(m * pre);
+    if (lane == 0) {
+      red[16] = q.s;
+      red[17] = q.r;
+    }
+  }
+  __syncthreads();
+  return RowQuant(red[16], red[17]);
+}
 
 // Round half to even of the FP32 product, two equivalent ways (bit-identical
 // codes; the kernel picks the one whose pipe has room):
