@@ -241,7 +241,7 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
   }
   // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
   const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, red, 0.0625f)
-                                 : RowQuant(cluster_pair_absmax(cta_absmax(amax, red), xred) * 0.0625f);
+                                 : cluster_rowquant(amax, red, xred, 0.0625f);
   if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
   const float mult = rq.r * 0.0625f;           // fp32(z * (r / 16)) == fp32((z / 16) * r)
@@ -377,7 +377,7 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
     }
   }
   const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, red, 1.0f)
-                                 : RowQuant(cluster_pair_absmax(cta_absmax(amax, red), xred));
+                                 : cluster_rowquant(amax, red, xred, 1.0f);
   if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
 #pragma unroll

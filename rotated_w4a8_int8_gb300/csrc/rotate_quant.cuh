@@ -145,38 +145,7 @@ __device__ __forceinline__ void scale_cols(BlockCols& c, float f) {
   }
 }
 
-// Row absmax over the CTA.  `red` holds one float per warp.
-__device__ __forceinline__ float cta_absmax(float local, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
-  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  if ((threadIdx.x & 31) == 0) red[warp] = local;
-  __syncthreads();
-  float m = 0.f;
-  for (int w = 0; w < nwarps; ++w) m = fmaxf(m, red[w]);
-  return m;
-}
-
-// Row absmax when a row is split over the two CTAs of a cluster: each CTA
-// holds its partial maximum (already reduced over the CTA); the two partials
-// are exchanged through distributed shared memory.  `xred` is this CTA's
-// exchange slot.  Every thread of both CTAs must call it; afterwards each
-// thread must call cluster_exit_wait() once before the CTA exits.
-__device__ __forceinline__ float cluster_pair_absmax(float cta_max, float* xred) {
-  if (threadIdx.x == 0) *xred = cta_max;
-  __syncwarp();
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-  uint32_t rank, local = static_cast<uint32_t>(__cvta_generic_to_shared(xred)), remote;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank ^ 1u));
-  float peer;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(peer) : "r"(remote) : "memory");
-  __syncwarp();
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");   // done reading the peer
-  return fmaxf(cta_max, peer);
-}
-
-// Completes cluster_pair_absmax: the peer may read this CTA's slot until here.
+// Completes cluster_rowquant: the peer may read this CTA's slot until here.
 __device__ __forceinline__ void cluster_exit_wait() {
   __syncwarp();
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -223,6 +192,46 @@ __device__ __forceinline__ RowQuant cta_rowquant(float local, float* red, float 
   }
   __syncthreads();
   return RowQuant(red[16], red[17]);
+}
+
+// The same for a row split over the two CTAs of a cluster: warp 0 reduces
+// this CTA's per-warp maxima and publishes the CTA maximum in xred[0]; after
+// a cluster barrier it reads the peer's, computes s and r and leaves them in
+// xred[2], xred[3] for the CTA.  Every thread of both CTAs must call it and
+// then call cluster_exit_wait() once before the CTA exits (the peer may read
+// xred[0] until then).
+__device__ __forceinline__ RowQuant cluster_rowquant(float local, float* red, float* xred, float pre) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  if (lane == 0) red[warp] = local;
+  __syncthreads();
+  float m = 0.f;
+  if (warp == 0) {
+    m = lane < nwarps ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) xred[0] = m;
+  }
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (warp == 0) {
+    uint32_t rank, remote;
+    const uint32_t local_addr = static_cast<uint32_t>(__cvta_generic_to_shared(xred));
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank ^ 1u));
+    float peer;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(peer) : "r"(remote) : "memory");
+    const RowQuant q(fmaxf(m, peer) * pre);
+    if (lane == 0) {
+      xred[2] = q.s;
+      xred[3] = q.r;
+    }
+  }
+  __syncwarp();
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");   // done reading the peer
+  __syncthreads();
+  return RowQuant(xred[2], xred[3]);
 }
 
 // Round half to even of the FP32 product, two equivalent ways (bit-identical
