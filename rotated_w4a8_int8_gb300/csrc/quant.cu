@@ -240,7 +240,7 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
     if (active) amax = absmax_cols(amax, c[i]);
   }
   // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
-  const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, red, 0.0625f)
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant<!SWIGLU>(amax, red, 0.0625f)
                                  : cluster_rowquant(amax, red, xred, 0.0625f);
   if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
@@ -376,7 +376,7 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
       amax = absmax_cols(amax, c[i]);
     }
   }
-  const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, red, 1.0f)
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant<true>(amax, red, 1.0f)
                                  : cluster_rowquant(amax, red, xred, 1.0f);
   if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);

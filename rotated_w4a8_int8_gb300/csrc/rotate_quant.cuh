@@ -169,21 +169,36 @@ struct RowQuant {
   __device__ __forceinline__ RowQuant(float s_, float r_) : s(s_), r(r_) {}
 };
 
+// Maximum over the warp of a non-negative float.  REDUX: non-negative floats
+// order like their bit patterns, so the integer warp reduction (one
+// instruction) applies; otherwise five shuffle-and-max steps.  Both give the
+// same value; the kernels take the form that measured faster for them (the
+// SwiGLU kernel was 3% slower with the integer reduction, the others 2.5-6%
+// faster).
+template <bool REDUX>
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+  if constexpr (REDUX) {
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+  } else {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+  }
+}
+
 // Row absmax and quantiser of a row held by one CTA, set up once: warp 0
 // reduces the per-warp maxima and computes s and r from amax * pre; every
 // thread reads them after a second barrier.  Cheaper than every warp
 // reducing the maxima and computing the division and the reciprocal itself.
 // `red` holds one float per warp plus s and r at [16], [17].
+template <bool REDUX>
 __device__ __forceinline__ RowQuant cta_rowquant(float local, float* red, float pre) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
+  local = warp_max_nonneg<REDUX>(local);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   if (lane == 0) red[warp] = local;
   __syncthreads();
   if (warp == 0) {
-    float m = lane < nwarps ? red[lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float m = warp_max_nonneg<REDUX>(lane < nwarps ? red[lane] : 0.f);
     const RowQuant q(m * pre);
     if (lane == 0) {
       red[16] = q.s;
@@ -201,16 +216,13 @@ __device__ __forceinline__ RowQuant cta_rowquant(float local, float* red, float 
 // then call cluster_exit_wait() once before the CTA exits (the peer may read
 // xred[0] until then).
 __device__ __forceinline__ RowQuant cluster_rowquant(float local, float* red, float* xred, float pre) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) local = fmaxf(local, __shfl_xor_sync(0xffffffffu, local, o));
+  local = warp_max_nonneg<true>(local);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   if (lane == 0) red[warp] = local;
   __syncthreads();
   float m = 0.f;
   if (warp == 0) {
-    m = lane < nwarps ? red[lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    m = warp_max_nonneg<true>(lane < nwarps ? red[lane] : 0.f);
     if (lane == 0) xred[0] = m;
   }
   __syncwarp();
