@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from the ncu capture
 # summarised in profiles/gemm_tcgen05_qkv.md; valid only while code_sha16(gemm.cu) equals this
 # (the hash ignores comments; otherwise the bench line reports traffic as null).
-GEMM_TRAFFIC = {"sha256_16": "a160da7c3a25735b", "bytes": 2979521792 + 912784640}
+GEMM_TRAFFIC = {"sha256_16": "67114e11caa6a2e2", "bytes": 3029191168 + 905975296}
 
 
 def code_sha16(path: str) -> str:
@@ -797,7 +797,7 @@ def main():
                              if args.overlap else "NVFP4 weight prep + act rotation/S8 + GEMM per step"),
                    "l2": f"flushed before every step ({flush_buf.numel() * 4 >> 20} MiB write)",
                    "parallelism": f"replicas x{world}",
-                   "arith": "S8 codes held as FP16 on tcgen05 kind::f16, exact int32 via 512-K FP32 chunks; "
+                   "arith": "S8 codes held as FP16 on tcgen05 kind::f16, exact int32 via 1024-K FP32 chunks; "
                             "FP32 rotation"},
         "ms_per_layer": ms_step,
         "ms_per_layer_serial": serial_ms,

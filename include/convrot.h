@@ -37,7 +37,7 @@
  * (CONVROT_CODES_F16, two bytes per code).  convrot_gemm reads the FP16
  * form: sm_103a tensor cores have no 8-bit integer MMA, so the GEMM runs the
  * FP16 tensor-core path, whose FP32 accumulation of these integer products
- * is exact, and it converts to int32 every 512 K.  The int32 accumulator is
+ * is exact, and it converts to int32 every 1024 K.  The int32 accumulator is
  * therefore bit-exact.
  */
 #ifndef CONVROT_H

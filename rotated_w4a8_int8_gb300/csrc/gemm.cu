@@ -13,8 +13,9 @@
 // GB300 design.  sm_103a has no 8-bit integer tcgen05 MMA, so the S8 codes
 // arrive stored as FP16 integers and the product runs on tcgen05.mma
 // kind::f16 with FP32 accumulation in tensor memory.  Products are at most
-// 127^2 and a 512-deep partial sum at most 127^2 * 512 < 2^23, so every FP32
-// partial sum is an exact integer.  The K loop is therefore cut into 512-wide
+// 127^2 and a 1024-deep partial sum at most 127^2 * 1024 = 16,516,096 < 2^24,
+// so every FP32 partial sum is an exact integer (tests drive running sums
+// that are odd and above 2^23).  The K loop is therefore cut into 1024-wide
 // chunks, each accumulated afresh in one of two TMEM buffers; epilogue warps
 // convert each finished chunk to int32 (exact) and add it to per-thread int32
 // registers while the tensor core fills the other buffer.
@@ -50,7 +51,7 @@ namespace crgemm {
 
 constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int STAGES = 4;
-constexpr int KCHUNK_STEPS = 8;                  // 8 * 64 = 512 K per exact FP32 chunk
+constexpr int KCHUNK_STEPS = 16;                 // 16 * 64 = 1024 K per exact FP32 chunk
 constexpr int A_BYTES = BM * BK * 2;             // 16 KiB
 constexpr int B_BYTES = BN * BK * 2;             // 32 KiB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -481,7 +482,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            // the FP32 value is an exact integer below 2^23: conversion is exact
+            // the FP32 value is an exact integer below 2^24: conversion is exact
             acc[g * 32 + j] += __float2int_rn(__uint_as_float(r[j]));
           }
         }

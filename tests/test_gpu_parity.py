@@ -256,9 +256,12 @@ def test_gemm_int32_bit_exact(M, N, Kp):
     assert np.array_equal(acc.cpu().numpy().astype(np.int64), oracle.int_gemm(qa, qw))
 
 
-@pytest.mark.parametrize("pattern", ["all_max", "alternating", "max_minus"])
+@pytest.mark.parametrize("pattern", ["all_max", "alternating", "max_minus", "odd_groups"])
 def test_gemm_int32_exact_at_extremes(pattern):
-    # partial sums reach 127^2 * 512 inside a chunk and 127^2 * 20480 in total
+    # partial sums reach 127^2 * 1024 inside a chunk and 127^2 * 20480 in total;
+    # "odd_groups" makes every 16-term group sum odd (15 * 127^2 + 127 * 126),
+    # so the running sums inside a chunk are odd and pass 2^23: an FP32
+    # accumulation that dropped a low bit above 2^23 would show
     import rotated_w4a8_int8_gb300 as cr
     M, N, Kp = 130, 260, 20480
     qa = np.full((M, Kp), 127, np.int8)
@@ -269,6 +272,9 @@ def test_gemm_int32_exact_at_extremes(pattern):
     elif pattern == "max_minus":
         qw[:] = -127
         qa[:, -1] = 126
+    elif pattern == "odd_groups":
+        qw[:, 15::16] = 126
+        qa[1::2, :] = -127
     acc = torch.zeros((M, N), dtype=torch.int32, device=DEV)
     cr.gemm_i32(f16_codes_from_np(qa), f16_codes_from_np(qw), acc)
     assert np.array_equal(acc.cpu().numpy().astype(np.int64), oracle.int_gemm(qa, qw))
