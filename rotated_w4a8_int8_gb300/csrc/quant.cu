@@ -392,8 +392,12 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
 
 // Kernel 1: one CTA per weight row, or (SPLIT == 2) a cluster of two CTAs
 // per row, each owning half of the row's blocks.
+// With one block per slot the kernel is held to 40 registers (at least 3 CTAs
+// of 512 threads per SM): 7 CTAs of a 21-block row then fit an SM instead of
+// 6, for a 4-byte spill, which measured 2-6% faster.  Two blocks per slot need
+// their registers.
 template <int NBMAX, bool W16, int SPLIT>
-__global__ void __launch_bounds__(kMaxThreads)
+__global__ void __launch_bounds__(kMaxThreads, NBMAX == 1 ? 3 : 1)
 prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restrict__ w_sf,
                       const float* __restrict__ tscale, int N, int K, int K_s, int nblocks, int S,
                       void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
