@@ -49,6 +49,9 @@ ACT_CASES = [
     ("k1", synth.Workload("k1", 5, 1, 8, "bf16", "bf16", False, 0.0, 1.0, 13)),
     ("max_kp", synth.Workload("maxkp", 3, 65536, 8, "bf16", "bf16", False, 0.01, 20.0, 17)),
     ("max_kp_swiglu", synth.Workload("maxkps", 2, 65536, 8, "bf16", "bf16", True, 0.0, 1.0, 18)),
+    # rows split over a CTA pair with one block per slot (16384 < K_p <= 32768), SwiGLU and FP16 inputs
+    ("split_swiglu", synth.Workload("spsw", 6, 20480, 8, "bf16", "bf16", True, 0.0, 1.0, 26)),
+    ("split_fp16_ragged", synth.Workload("spf16", 5, 17000, 8, "fp16", "fp32", False, 0.01, 20.0, 27)),
 ]
 
 
@@ -368,6 +371,7 @@ PS_CASES = [
     ("bf16_swiglu", synth.Workload("ps1", 70, 1000, 300, "bf16", "bf16", True, 0.0, 1.0, 23)),
     ("fp16_plain", synth.Workload("ps2", 130, 768, 520, "fp16", "fp32", False, 0.02, 20.0, 24)),
     ("fp32_in", synth.Workload("ps3", 33, 512, 257, "fp32", "fp16", False, 0.0, 1.0, 25)),
+    ("split_rows", synth.Workload("ps4", 9, 20000, 130, "bf16", "bf16", False, 0.01, 20.0, 28)),
 ]
 
 
