@@ -40,6 +40,15 @@ design notes):
   * A row whose FP32 scale is zero, or whose FP32 reciprocal overflows, is a
     degenerate row: its scale is stored as 0 and all of its codes are 0.
   * The activation side uses the same quantiser as the weight side.
+  * Channel pre-scales ("Pre-scales and SwiGLU run before rotation") multiply
+    the layer's input channel-wise after SwiGLU and before the rotation; the
+    optional bias is added in FP32 before the output rounding.
+
+Pins: every step is checked against something other than this file in the
+oracle pin tests (the OCP tables, closed forms of the rotation, invariance
+of the rotated product, brute-force integer GEMMs, single-rounding output
+cases, the pages' printed 1.31% / 1.39% added error).  Exact reproduction of
+the pages' own codes is parity unpinned: the pages print no vectors.
 """
 from __future__ import annotations
 
