@@ -303,9 +303,13 @@ class E2EPipeline:
     buffered and guarded by events.
     """
 
-    def __init__(self, layer: Layer, copy_streams: int = 2):
+    def __init__(self, layer: Layer, copy_streams: int = 2, host_poll: bool = True):
         import torch
         self.L = layer
+        # The host polls the pipeline's events instead of sleeping in a blocking
+        # wait: on some boxes the device-to-host copies ran at a fraction of the
+        # link rate once the host thread went idle.
+        self.host_poll = host_poll
         self.torch = torch
         dev = layer.x.device
         self.s_in = torch.cuda.Stream(dev)
@@ -334,6 +338,10 @@ class E2EPipeline:
         for i in range(steps):
             b = self.bufs[i % 2]
             k = i % 2
+            if self.host_poll and run_done[k] is not None:
+                # the host stays at most two steps ahead, polling (not sleeping)
+                while not run_done[k].query():
+                    pass
             with torch.cuda.stream(self.s_in):
                 if run_done[k] is not None:
                     self.s_in.wait_event(run_done[k])
@@ -370,6 +378,9 @@ class E2EPipeline:
         self.s_out.wait_stream(self.s_in)
         self.s_out.wait_stream(self.s_run)
         t1.record(self.s_out)
+        if self.host_poll:
+            while not t1.query():
+                pass
         t1.synchronize()
         return t0.elapsed_time(t1)
 
