@@ -4,7 +4,7 @@
  * The layer (ComfyUI Turing Utils page on comfy.icu, node list, entry "Load
  * ConvRot DiT and Load ConvRot CLIP also accept ComfyUI-native nvfp4 layers")
  * keeps its weights in NVFP4, applies the same 256-point block rotation
- * ("paired ConvRot256") to the activations and to the decoded weights,
+ * (paired ConvRot256) to the activations and to the decoded weights,
  * quantises both to row-scaled S8 and multiplies them with an integer GEMM
  * whose epilogue dequantises to BF16 / FP16 / FP32:
  *
@@ -74,8 +74,8 @@ const char* convrot_status_string(int status);
 
 /*
  * Weight preparation: NVFP4 decode + ConvRot256 rotation in FP32 + row-scaled
- * S8 quantisation (the page's "NVFP4 decode, FP32 weight rotation and S8
- * quantization are fused"; the stored NVFP4 bytes are only read).
+ * S8 quantisation, one fused step as the page describes it; the stored NVFP4
+ * bytes are only read.
  *
  *   w_fp4   [N][K_s/2] uint8, K_s = ceil(K/16)*16, rows contiguous.  Byte j of
  *           a row holds element 2j in its low nibble, 2j+1 in its high nibble;
@@ -102,9 +102,9 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
 
 /*
  * Activation quantisation: optional SwiGLU prologue, optional channel
- * pre-scales, then ConvRot256 rotation in FP32 and row-scaled S8 quantisation
- * (the page's "Pre-scales and SwiGLU run before rotation" and "SwiGLU is
- * fused with rotation/A8 quantization").
+ * pre-scales, then ConvRot256 rotation in FP32 and row-scaled S8 quantisation.
+ * On the page both the pre-scales and SwiGLU come before the rotation, and
+ * SwiGLU is fused into the activation rotation and quantisation.
  *
  *   x       [M][ld_x] in x_dtype (BF16 / FP16 / FP32).  swiglu == 0: columns
  *           0..K-1 are the input.  swiglu != 0: columns 0..K-1 are the gate
@@ -130,9 +130,9 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
                       float* a_scale, cudaStream_t stream);
 
 /*
- * Integer GEMM with the dequantising epilogue (the page's "row-scaled INT8
- * Tensor Core GEMM"; the rescale happens inside the GEMM so no int32 matrix
- * is ever written).
+ * Integer GEMM with the dequantising epilogue (the page's tensor-core INT8
+ * GEMM over row-scaled operands; the rescale happens inside the GEMM so no
+ * int32 matrix is ever written).
  *
  *   a_q     [M][ld_aq] FP16-stored S8 codes of the rotated activations.
  *   w_q     [N][ld_wq] FP16-stored S8 codes of the rotated weights.
@@ -158,8 +158,8 @@ int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale,
 /*
  * W8A8 with resident weights: widens S8 codes (CONVROT_CODES_S8, e.g. weight
  * codes prepared once and kept at one byte each) into the FP16-held codes
- * that convrot_gemm reads (the page's "W8A8 controls use the same
- * NVFP4-derived rotated S8 weights").
+ * that convrot_gemm reads.  The page's W8A8 comparison uses exactly these
+ * rotated S8 weights derived from the NVFP4 checkpoint.
  *
  *   src  [rows][ld_src] int8, 16-byte aligned, ld_src a multiple of 16.
  *   dst  [rows][ld_dst] FP16, 16-byte aligned, ld_dst a multiple of 8.

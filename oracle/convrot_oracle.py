@@ -23,15 +23,17 @@ section: gate, value = fc1(x).chunk(2); hidden = swish(gate) * value) runs
 on the activations before the rotation, without intermediate rounding.
 
 Precision: FP64 throughout, except where the method fixes FP32: the rotated
-operands are held in FP32 ("FP32 weight rotation"; FP16 inputs use "FP32
-rotation/quantization"), and the S8 code of every element is decided in FP32
-(FP32 scale, FP32 reciprocal, FP32 product, round half to even).
+operands are held in FP32 (the page rotates the weights in FP32, and rotates
+and quantises FP16 inputs in FP32), and the S8 code of every element is
+decided in FP32 (FP32 scale, FP32 reciprocal, FP32 product, round half to
+even).
 
 Readings where the pages are silent (each listed with its reason in the
 design notes):
-  * ConvRot256's matrix is never printed.  The modelpad glossary calls it a
-    Hadamard matrix ("an orthogonal matrix of +-1"); we take the normalised
-    256-point Sylvester Walsh-Hadamard matrix R = H_256 / 16.
+  * ConvRot256's matrix is never printed.  The modelpad glossary names a
+    Hadamard rotation, i.e. an orthogonal matrix with entries of +-1 before
+    normalisation; we take the normalised 256-point Sylvester Walsh-Hadamard
+    matrix R = H_256 / 16.
   * E2M1 / E4M3 follow the OCP Microscaling and OFP8 definitions (E4M3 "FN":
     bias 7, no infinities, S.1111.111 is NaN).
   * Nibble order: byte j of a row holds element 2j in its low nibble.
@@ -40,9 +42,10 @@ design notes):
   * A row whose FP32 scale is zero, or whose FP32 reciprocal overflows, is a
     degenerate row: its scale is stored as 0 and all of its codes are 0.
   * The activation side uses the same quantiser as the weight side.
-  * Channel pre-scales ("Pre-scales and SwiGLU run before rotation") multiply
-    the layer's input channel-wise after SwiGLU and before the rotation; the
-    optional bias is added in FP32 before the output rounding.
+  * Channel pre-scales (which the page places before the rotation, like
+    SwiGLU) multiply the layer's input channel-wise after SwiGLU and before
+    the rotation; the optional bias is added in FP32 before the output
+    rounding.
 
 Pins: every step is checked against something other than this file in the
 oracle pin tests (the OCP tables, closed forms of the rotation, invariance
@@ -289,9 +292,10 @@ def quant_act(x_storage, x_dtype: str, K: int, swiglu_flag: bool = False, pre_sc
     """(SwiGLU ->) (channel pre-scale ->) pad -> rotate -> row-scaled S8.
 
     Channel pre-scales multiply the layer's input h[:, k] by p[k] before the
-    rotation ("Pre-scales and SwiGLU run before rotation"; "Channel pre-scales
-    retain the correct unfused ordering": the scale belongs to this layer's
-    input, so it follows the SwiGLU that produces that input).
+    rotation.  The page places pre-scales and SwiGLU before the rotation and
+    keeps the order of the unfused computation; read here as: the scale
+    belongs to this layer's input, so it follows the SwiGLU that produces
+    that input.
     Returns (q_a, s_a).
     """
     x = storage_to_f64(x_storage, x_dtype)

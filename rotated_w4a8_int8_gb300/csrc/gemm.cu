@@ -3,10 +3,10 @@
 // convrot_gemm_i32 and convrot_device_error.
 //
 // What it computes (ComfyUI Turing Utils page on comfy.icu, node list, entry
-// "Load ConvRot DiT ... nvfp4": "row-scaled INT8 Tensor Core GEMM", FP16 /
-// BF16 / FP32 outputs, N tails; MiniMax-H3 explainer on modelpad.app: the
-// rescale lives inside the matmul so the int32 intermediate never touches
-// memory):
+// "Load ConvRot DiT ... nvfp4": an INT8 tensor-core GEMM over row-scaled
+// operands, FP16 / BF16 / FP32 outputs, logical N tails; MiniMax-H3
+// explainer on modelpad.app: the rescale lives inside the matmul so the
+// int32 intermediate never touches memory):
 //     acc[m, n] = sum_k q_a[m, k] * q_w[n, k]            (exact int32)
 //     y[m, n]   = fp32(acc) * s_a[m] * s_w[n]  -> out dtype
 //

@@ -600,8 +600,8 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
 }
 
 // ------------------------------------------------------------------ S8 -> FP16 code widening
-// W8A8 with resident weights (the page's "W8A8 controls use the same
-// NVFP4-derived rotated S8 weights"): weights kept as 1-byte S8 codes are
+// W8A8 with resident weights (the page's W8A8 comparison runs on these same
+// rotated S8 weights derived from NVFP4): weights kept as 1-byte S8 codes are
 // widened to the FP16-held codes the GEMM reads.  Each thread converts 16
 // codes (one 16-byte load, two 16-byte stores); rows and pitches must keep
 // those accesses aligned.
