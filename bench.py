@@ -9,10 +9,12 @@ call as in the layer's single runtime path.  Inputs are seeded synthetic data
 of the workload's shape and distribution, resident in HBM before timing; L2 is
 flushed (a write larger than L2) before every timed step.
 
-Prints ONE JSON line (rank 0).  `value` is effective TOPS = 2 M N K / t summed
-over ranks (replicas: every rank runs the full layer on its own GPU).
+Prints ONE JSON line.  `value` is effective TOPS = 2 M N K / t.  The layer
+runs on one GPU: its GEMM loads operand tiles with cluster-multicast TMA over
+tensor maps of this GPU's own memory, so bench.py refuses --gpus > 1 and any
+launch with WORLD_SIZE > 1 (the CPU reference arm excepted).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--steps K] [--warmup W] [--impl ours|reference]
 """
 from __future__ import annotations
 
@@ -41,9 +43,9 @@ METRIC = "ms/layer and effective INT8 TOPS at M=19989 (QKV, FFN-down); % of INT8
 # the pages' QKV layer time on an A40 at M=19989 (context, another machine)
 PAGES_QKV_MS = 25.08
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from the ncu capture
-# summarised in profiles/gemm_tcgen05_qkv.md; valid only while code_sha16(gemm.cu) equals this
-# (the hash ignores comments; otherwise the bench line reports traffic as null).
+# DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from an ncu capture of
+# this kernel; valid only while code_sha16(gemm.cu) equals this (the hash ignores comments;
+# otherwise the bench line reports traffic as null).
 GEMM_TRAFFIC = {"sha256_16": "67114e11caa6a2e2", "bytes": 3029191168 + 905975296}
 
 
@@ -70,13 +72,18 @@ def load_peaks():
 
 # ---------------------------------------------------------------- workload sizes
 def layer_sizes(wl: synth.Workload):
+    """Work of one layer.  act_alg / w_alg are the algorithmic bytes of the
+    two quantisation kernels with one-byte S8 codes (inputs read once, codes
+    and scales written once); act_bytes / w_bytes are the bytes the kernels
+    actually move, with the codes held as FP16 (two bytes) for the GEMM."""
     Kp = -(-wl.K // 256) * 256
     Ks = synth.stored_k(wl.K)
     esz = {"bf16": 2, "fp16": 2, "fp32": 4}
-    act_bytes = wl.M * wl.k_in * esz[wl.x_dtype] + wl.M * Kp * 2 + 4 * wl.M
-    w_bytes = wl.N * Ks // 2 + wl.N * Ks // 16 + 4 + wl.N * Kp * 2 + 4 * wl.N
+    act_in = wl.M * wl.k_in * esz[wl.x_dtype]
+    w_in = wl.N * Ks // 2 + wl.N * Ks // 16
     return dict(Kp=Kp, Ks=Ks, ops=2.0 * wl.M * wl.N * wl.K, gemm_flops=2.0 * wl.M * wl.N * Kp,
-                act_bytes=act_bytes, w_bytes=w_bytes)
+                act_alg=act_in + wl.M * Kp + 4 * wl.M, w_alg=w_in + wl.N * Kp + 4 * wl.N,
+                act_bytes=act_in + wl.M * Kp * 2 + 4 * wl.M, w_bytes=w_in + 4 + wl.N * Kp * 2 + 4 * wl.N)
 
 
 # ---------------------------------------------------------------- clocks
@@ -130,21 +137,22 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-# ---------------------------------------------------------------- distributed
-def dist_setup(n_gpus: int):
-    import torch
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    return rank, world, local
+# ---------------------------------------------------------------- one GPU
+SINGLE_GPU_MSG = ("bench.py times the ConvRot layer on one GPU only: its GEMM issues cluster-multicast "
+                  "TMA loads over tensor maps of this GPU's own memory, and no run of this code may span "
+                  "two or more GPUs.  Token rows shard without any exchange (replicas), but that path is "
+                  "not run here.")
 
 
+def single_gpu_guard(n_gpus: int, world: int) -> None:
+    """Refuses a launch on more than one GPU (the product arm)."""
+    if n_gpus != 1 or world != 1:
+        raise SystemExit(f"refused: --gpus {n_gpus}, WORLD_SIZE {world}. " + SINGLE_GPU_MSG)
+
+
+# The job-level helpers below are kept general (max over ranks, sum of
+# replicas) and are exercised on the CPU by gloo tests; on the single GPU
+# that the benchmark runs they reduce to the identity.
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -582,6 +590,84 @@ def time_controls(wl: synth.Workload, dev, world, flush, warmup, steps=20):
     return out
 
 
+def time_library_controls(wl: synth.Workload, dev, flush, warmup, steps=20):
+    """Library controls, timed the way the layer's GEMM is (L2 flushed before
+    every call, CUDA events on the launching stream), off the product path:
+    - cublas_fp16: torch.matmul in FP16 on the GEMM's own shape (M x K_p) x
+      (K_p x N), the same tensor-core route and operand width as the layer's
+      GEMM;
+    - int8_mm: torch._int_mm (cuBLASLt S8 x S8 -> int32) on the same shape and
+      at 8192^3: the rate of the S8 tensor path this GPU offers through the
+      library, the denominator of an "INT8 roofline"."""
+    import torch
+    M, N, Kp = wl.M, wl.N, -(-wl.K // 256) * 256
+    g = torch.Generator(device=dev).manual_seed(7)
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(n):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / n
+
+    out = {}
+    A = torch.randint(-127, 128, (M, Kp), generator=g, device=dev).to(torch.float16)
+    B = torch.randint(-127, 128, (N, Kp), generator=g, device=dev).to(torch.float16)
+    ms = timed(lambda: torch.matmul(A, B.t()), steps)
+    out["cublas_fp16"] = {"shape": f"{M}x{N}x{Kp}", "ms": ms, "tflops": 2.0 * M * N * Kp / (ms / 1e3) / 1e12}
+    del A, B
+    torch.cuda.empty_cache()
+    for name, (m, n, k) in (("int8_mm", (M, N, Kp)), ("int8_mm_8192", (8192, 8192, 8192))):
+        try:
+            A8 = torch.randint(-127, 128, (m, k), generator=g, device=dev, dtype=torch.int8)
+            B8 = torch.randint(-127, 128, (n, k), generator=g, device=dev, dtype=torch.int8)
+            ms = timed(lambda: torch._int_mm(A8, B8.t()), 5)
+            out[name] = {"shape": f"{m}x{n}x{k}", "ms": ms, "tops": 2.0 * m * n * k / (ms / 1e3) / 1e12}
+            del A8, B8
+        except RuntimeError as e:            # not offered by this torch build
+            out[name] = {"shape": f"{m}x{n}x{k}", "unavailable": str(e).splitlines()[0][:200]}
+        torch.cuda.empty_cache()
+    return out
+
+
+def time_sustained(layer: "Layer", seconds: float, est_ms: float, bus, sm_count: int):
+    """Back-to-back layers for about `seconds` s with their own sampled clocks:
+    the regime of a long run (many DiT blocks in a row) in which the power cap
+    sets the clock.  Operands exceed the L2 (x 215 MB, codes 446 MB at QKV), so
+    no flush between layers."""
+    n = max(20, int(seconds * 1e3 / max(est_ms, 1e-3)))
+    r = time_layer(layer, n, 3, 1, lambda: None, ClockSampler(bus))
+    ms = r["total_ms"] / n
+    g_ms = statistics.mean(r["gemm_ms"])
+    clocks = r["clocks"] or {}
+    mhz = clocks.get("sm_mhz")
+    out = {"layers": n, "seconds": r["total_ms"] / 1e3, "ms_per_layer": ms,
+           "eff_tops": layer.sz["ops"] / (ms / 1e3) / 1e12, "gemm_ms": g_ms,
+           "gemm_tflops": layer.sz["gemm_flops"] / (g_ms / 1e3) / 1e12,
+           "quant_act_us": 1e3 * statistics.mean(r["act_ms"]),
+           "prepare_weight_us": 1e3 * statistics.mean(r["weight_ms"]), "clocks": clocks}
+    if mhz:
+        out["ms_x_mhz_per_layer"] = ms * mhz
+        out["tensor_pipe_peak_at_clock_tflops"] = tensor_pipe_peak(sm_count, mhz)
+    return out
+
+
+def tensor_pipe_peak(sm_count: int, mhz: float) -> float:
+    """Dense FP16/BF16 tensor-pipe peak at a given SM clock: 8192 FLOP per
+    clock per SM (one 128 x 256 x 16 MMA every 128 clocks)."""
+    return 8192.0 * sm_count * mhz * 1e6 / 1e12
+
+
 # ---------------------------------------------------------------- CPU oracle baseline
 class OracleSample:
     """The first m tokens x first n weight rows of a workload, generated once;
@@ -646,11 +732,22 @@ def reference_arm(args, wl):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sum(ts) / len(ts), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name} M={wl.M} K={wl.K} N={wl.N}", "sample": sample_txt},
+        "config": bench_config(wl, args.overlap),
         "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle",
                          "sample": sample_txt},
         "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def bench_config(wl: synth.Workload, overlap: int) -> dict:
+    """The workload description shared by both arms of the benchmark."""
+    return {"workload": f"{wl.name} M={wl.M} K={wl.K} N={wl.N} {wl.x_dtype}->{wl.out_dtype}",
+            "layer": ("NVFP4 weight prep on a second stream beside act rotation/S8, then GEMM, per step"
+                      if overlap else "NVFP4 weight prep + act rotation/S8 + GEMM per step"),
+            "l2": "flushed before every step (a write of twice the L2 size)",
+            "parallelism": "single GPU",
+            "arith": "S8 codes held as FP16 on tcgen05 kind::f16, exact int32 via 1024-K FP32 chunks; "
+                     "FP32 rotation"}
 
 
 # ---------------------------------------------------------------- main
@@ -674,6 +771,10 @@ def main():
                     help="also time the W8A8 / resident-weight controls and pre-scale+bias (0 to skip)")
     ap.add_argument("--ffn-block", type=int, default=1,
                     help="also time the FFN block fc1 -> SwiGLU/rotate/S8 -> fc2 (0 to skip)")
+    ap.add_argument("--sustained-s", type=float, default=4.0,
+                    help="seconds of back-to-back layers for the sustained-clock leg (0 to skip)")
+    ap.add_argument("--library", type=int, default=1,
+                    help="also time the cuBLAS FP16 and cuBLASLt INT8 controls on the GEMM's shape (0 to skip)")
     ap.add_argument("--rows", type=int, default=0,
                     help="truncate M to this many tokens (small profiling case; not a bench line)")
     args = ap.parse_args()
@@ -686,13 +787,17 @@ def main():
         reference_arm(args, wl)
         return
 
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    single_gpu_guard(args.gpus, world)
+
     import torch
 
     import __graft_entry__
     __graft_entry__.build()
-    rank, world, local = dist_setup(args.gpus)
-    dev = torch.device("cuda", local)
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
     props = torch.cuda.get_device_properties(dev)
+    sm_count = int(props.multi_processor_count)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20))
     flush_buf = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
 
@@ -703,69 +808,76 @@ def main():
     if isinstance(bus, int):
         bus = None
     peaks, peaks_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
 
     layer = Layer(wl, dev)
     sz = layer.sz
-    r = time_layer(layer, args.steps, args.warmup, world, flush, None if args.overlap else ClockSampler(bus))
-    serial_ms = reduce_max(r["total_ms"], world) / args.steps
+    r = time_layer(layer, args.steps, args.warmup, 1, flush, None if args.overlap else ClockSampler(bus))
+    serial_ms = r["total_ms"] / args.steps
     if args.overlap:
-        ro = time_layer_overlapped(layer, args.steps, args.warmup, world, flush, ClockSampler(bus))
-        t_max = reduce_max(ro["total_ms"], world)
+        ro = time_layer_overlapped(layer, args.steps, args.warmup, 1, flush, ClockSampler(bus))
+        t_tot = ro["total_ms"]
         clocks = ro["clocks"]
     else:
-        t_max = reduce_max(r["total_ms"], world)
+        t_tot = r["total_ms"]
         clocks = r["clocks"]
-    ms_step = t_max / args.steps
-    value = aggregate_tops(sz["ops"], args.steps, t_max, world)
+    ms_step = t_tot / args.steps
+    value = aggregate_tops(sz["ops"], args.steps, t_tot, 1)
     g_ms = statistics.mean(r["gemm_ms"])
     a_ms = statistics.mean(r["act_ms"])
     w_ms = statistics.mean(r["weight_ms"])
     achieved = sz["gemm_flops"] / (g_ms / 1e3) / 1e12
-    peak_t = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gemm_src = os.path.join(ROOT, "rotated_w4a8_int8_gb300", "csrc", "gemm.cu")
     traffic = GEMM_TRAFFIC["bytes"] if GEMM_TRAFFIC["sha256_16"] == code_sha16(gemm_src) else None
+
+    def quant_kernel(us, alg, moved):
+        gbs = alg / (us / 1e6) / 1e9
+        return {"us": us, "alg_bytes": alg, "gbs": gbs, "hbm_frac": gbs / hbm,
+                "moved_bytes": moved, "moved_gbs": moved / (us / 1e6) / 1e9,
+                "moved_frac": moved / (us / 1e6) / 1e9 / hbm}
+
+    kernels = {
+        "prepare_weight": quant_kernel(1e3 * w_ms, sz["w_alg"], sz["w_bytes"]),
+        "quant_act": quant_kernel(1e3 * a_ms, sz["act_alg"], sz["act_bytes"]),
+        "gemm": {"ms": g_ms, "tflops": achieved},
+    }
 
     # end-to-end through the public API with host buffers
     e2e_value = e2e_ms = link = None
     h2d = layer.in_bytes
     d2h = layer.y.numel() * layer.y.element_size()
     if args.e2e_steps > 0:
-        e2e_ms, h2d, d2h, link = time_e2e(layer, args.e2e_steps, 3, world)
-        e2e_ms = reduce_max(e2e_ms, world)
-        e2e_value = aggregate_tops(sz["ops"], args.e2e_steps, e2e_ms, world)
+        e2e_ms, h2d, d2h, link = time_e2e(layer, args.e2e_steps, 3, 1)
+        e2e_value = aggregate_tops(sz["ops"], args.e2e_steps, e2e_ms, 1)
+    sustained = None
+    if args.sustained_s > 0:
+        sustained = time_sustained(layer, args.sustained_s, ms_step, bus, sm_count)
+        sustained["gemm_frac_of_sustained_peak"] = sustained["gemm_tflops"] / peak_sust
     if layer.cr.device_error() != 0:
         raise SystemExit("device timeout reported by the GEMM")
-
-    kernels = {
-        "prepare_weight": {"us": 1e3 * w_ms, "bytes": sz["w_bytes"],
-                           "gbs": sz["w_bytes"] / (w_ms / 1e3) / 1e9},
-        "quant_act": {"us": 1e3 * a_ms, "bytes": sz["act_bytes"],
-                      "gbs": sz["act_bytes"] / (a_ms / 1e3) / 1e9},
-        "gemm": {"ms": g_ms, "tflops": achieved},
-    }
-    for k in ("prepare_weight", "quant_act"):
-        kernels[k]["hbm_frac"] = kernels[k]["gbs"] / hbm
     del layer
     torch.cuda.empty_cache()
+
+    library = time_library_controls(wl, dev, flush, args.warmup) if args.library else None
 
     secondary = None
     if args.secondary:
         wl2 = synth.WORKLOADS[args.secondary]
         l2y = Layer(wl2, dev)
-        r2 = time_layer(l2y, max(10, args.steps // 4), args.warmup, world, flush)
+        r2 = time_layer(l2y, max(10, args.steps // 4), args.warmup, 1, flush)
         s2 = l2y.sz
-        ms2 = reduce_max(r2["total_ms"], world) / len(r2["step_ms"])
+        ms2 = r2["total_ms"] / len(r2["step_ms"])
         g2 = statistics.mean(r2["gemm_ms"])
-        a2 = statistics.mean(r2["act_ms"])
-        w2 = statistics.mean(r2["weight_ms"])
+        a2 = 1e3 * statistics.mean(r2["act_ms"])
+        w2 = 1e3 * statistics.mean(r2["weight_ms"])
         secondary = {"workload": f"{wl2.name} M={wl2.M} K={wl2.K} (SwiGLU input {wl2.k_in}) N={wl2.N}"
                      if wl2.swiglu else f"{wl2.name} M={wl2.M} K={wl2.K} N={wl2.N}",
                      "ms_per_layer": ms2, "eff_tops": s2["ops"] / (ms2 / 1e3) / 1e12,
                      "gemm_ms": g2, "gemm_tflops": s2["gemm_flops"] / (g2 / 1e3) / 1e12,
-                     "quant_act_us": 1e3 * a2, "quant_act_gbs": s2["act_bytes"] / (a2 / 1e3) / 1e9,
-                     "prepare_weight_us": 1e3 * w2,
-                     "prepare_weight_gbs": s2["w_bytes"] / (w2 / 1e3) / 1e9,
+                     "quant_act": quant_kernel(a2, s2["act_alg"], s2["act_bytes"]),
+                     "prepare_weight": quant_kernel(w2, s2["w_alg"], s2["w_bytes"]),
                      "pages_a40_ms": 19.49}
         del l2y
         torch.cuda.empty_cache()
@@ -774,57 +886,69 @@ def main():
     for name in [n for n in args.others.split(",") if n]:
         wlo = synth.WORKLOADS[name]
         lo = Layer(wlo, dev)
-        ro = time_layer(lo, 20, args.warmup, world, flush)
+        ro = time_layer(lo, 20, args.warmup, 1, flush)
         so = lo.sz
-        mso = reduce_max(ro["total_ms"], world) / len(ro["step_ms"])
+        mso = ro["total_ms"] / len(ro["step_ms"])
+        ao = 1e3 * statistics.mean(ro["act_ms"])
+        wo = 1e3 * statistics.mean(ro["weight_ms"])
         others[name] = {"workload": f"M={wlo.M} K={wlo.K} N={wlo.N} {wlo.x_dtype}->{wlo.out_dtype}",
                         "ms_per_layer": mso, "eff_tops": so["ops"] / (mso / 1e3) / 1e12,
                         "gemm_tflops": so["gemm_flops"] / (statistics.mean(ro["gemm_ms"]) / 1e3) / 1e12,
-                        "quant_act_gbs": so["act_bytes"] / (statistics.mean(ro["act_ms"]) / 1e3) / 1e9,
-                        "prepare_weight_gbs": so["w_bytes"] / (statistics.mean(ro["weight_ms"]) / 1e3) / 1e9}
+                        "quant_act_us": ao, "quant_act_hbm_frac": so["act_alg"] / (ao / 1e6) / 1e9 / hbm,
+                        "prepare_weight_us": wo, "prepare_weight_hbm_frac": so["w_alg"] / (wo / 1e6) / 1e9 / hbm}
         del lo
         torch.cuda.empty_cache()
 
     ffn = None
     if args.ffn_block:
-        ffn = time_ffn_block(dev, world, flush, args.warmup)
+        ffn = time_ffn_block(dev, 1, flush, args.warmup)
     controls = None
     if args.controls:
-        controls = time_controls(wl, dev, world, flush, args.warmup)
+        controls = time_controls(wl, dev, 1, flush, args.warmup)
 
     cpu = None
-    if rank == 0 and world == 1 and args.cpu_budget > 0:
+    if args.cpu_budget > 0:
         cpu = cpu_baseline(wl, args.cpu_budget)
 
-    if rank != 0:
-        return
+    mhz = (clocks or {}).get("sm_mhz")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst, "traffic": traffic,
+                "kernel": "gemm_kernel (tcgen05 kind::f16)",
+                "peak_source": f"{peaks_src} bf16_tflops (burst: the GEMM is timed in short steps; "
+                               f"FP16 runs at the BF16 rate)",
+                "work_per_launch": f"2*M*N*K_p = {sz['gemm_flops']:.4e} FLOP",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one full-size launch"}
+    if mhz:
+        pipe = tensor_pipe_peak(sm_count, mhz)
+        roofline["tensor_pipe_peak_at_clock"] = pipe
+        roofline["tensor_pipe_frac"] = achieved / pipe
+    if library and "tflops" in library.get("cublas_fp16", {}):
+        roofline["vs_cublas_fp16_same_shape"] = achieved / library["cublas_fp16"]["tflops"]
+    if library and "tops" in library.get("int8_mm", {}):
+        roofline["int8_library_tops_same_shape"] = library["int8_mm"]["tops"]
+        roofline["vs_int8_library_same_shape"] = achieved / library["int8_mm"]["tops"]
+
     line = {
-        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": value / world / (sz["ops"] / (PAGES_QKV_MS / 1e3) / 1e12),
+        "scaling": "weak", "vs_baseline": value / (sz["ops"] / (PAGES_QKV_MS / 1e3) / 1e12),
         "dtype": "s8", "data": "synthetic",
-        "config": {"workload": f"{wl.name} M={wl.M} K={wl.K} N={wl.N} {wl.x_dtype}->{wl.out_dtype}",
-                   "layer": ("NVFP4 weight prep on a second stream beside act rotation/S8, then GEMM, per step"
-                             if args.overlap else "NVFP4 weight prep + act rotation/S8 + GEMM per step"),
-                   "l2": f"flushed before every step ({flush_buf.numel() * 4 >> 20} MiB write)",
-                   "parallelism": f"replicas x{world}",
-                   "arith": "S8 codes held as FP16 on tcgen05 kind::f16, exact int32 via 1024-K FP32 chunks; "
-                            "FP32 rotation"},
+        "config": bench_config(wl, args.overlap),
         "ms_per_layer": ms_step,
         "ms_per_layer_serial": serial_ms,
         "kernels": kernels,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": achieved / peak_t, "traffic": traffic,
-                     "kernel": "gemm (tcgen05 kind::f16)",
-                     "peak_source": f"{peaks_src} bf16_tflops_sustained (FP16 = BF16 rate)",
-                     "work_per_launch": f"2*M*N*K_p = {sz['gemm_flops']:.4e} FLOP"},
+        "roofline": roofline,
         "hbm_peak_gbs": hbm,
+        "hbm_note": ("quant kernels: hbm_frac on algorithmic bytes with 1-byte S8 codes; moved_* on the bytes "
+                     "actually moved (codes held as FP16 for the GEMM)"),
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "pipelined": "streams: copy-in, kernels, copy-out split over 2 copy streams",
                 "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None,
                 "host_link_gbs": link},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
+        "sustained": sustained,
+        "library": library,
         "cpu_baseline": cpu,
         "secondary": secondary,
         "others": others,

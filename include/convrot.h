@@ -1,9 +1,9 @@
 /*
  * convrot.h -- C ABI of the ConvRot W4A8 linear layer for GB300 (sm_103a).
  *
- * The layer (ComfyUI Turing Utils page on comfy.icu, node list, entry "Load
- * ConvRot DiT and Load ConvRot CLIP also accept ComfyUI-native nvfp4 layers")
- * keeps its weights in NVFP4, applies the same 256-point block rotation
+ * The layer (ComfyUI Turing Utils page on comfy.icu, node list, the entry on
+ * the ConvRot DiT / CLIP loaders reading native NVFP4 layers; cited below as
+ * "the NVFP4 loader entry") keeps its weights in NVFP4, applies the same 256-point block rotation
  * (paired ConvRot256) to the activations and to the decoded weights,
  * quantises both to row-scaled S8 and multiplies them with an integer GEMM
  * whose epilogue dequantises to BF16 / FP16 / FP32:
@@ -74,8 +74,17 @@ const char* convrot_status_string(int status);
 
 /*
  * Weight preparation: NVFP4 decode + ConvRot256 rotation in FP32 + row-scaled
- * S8 quantisation, one fused step as the page describes it; the stored NVFP4
- * bytes are only read.
+ * S8 quantisation in one fused step.  Source: the NVFP4 loader entry's weight
+ * path -- the NVFP4 tensor is decoded, rotated in FP32 by the same ConvRot256
+ * as the activations and quantised per row with a rounded FP32 reciprocal of
+ * the row scale, and the serialised padding past K is skipped.  The stored
+ * NVFP4 bytes are only read.
+ *
+ * Row ranges: the call has no row-offset argument.  To prepare rows
+ * [n0, n0 + n) of a weight, pass w_fp4 + n0 * (K_s/2), w_sf + n0 * (K_s/16),
+ * w_q + n0 * ld_wq (in code elements) and w_scale + n0 with N = n; rows are
+ * independent, so the result equals that of the whole-weight call (the
+ * alignment rules below apply to the offset pointers).
  *
  *   w_fp4   [N][K_s/2] uint8, K_s = ceil(K/16)*16, rows contiguous.  Byte j of
  *           a row holds element 2j in its low nibble, 2j+1 in its high nibble;
@@ -103,8 +112,12 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
 /*
  * Activation quantisation: optional SwiGLU prologue, optional channel
  * pre-scales, then ConvRot256 rotation in FP32 and row-scaled S8 quantisation.
- * On the page both the pre-scales and SwiGLU come before the rotation, and
- * SwiGLU is fused into the activation rotation and quantisation.
+ * Source: the NVFP4 loader entry's activation path -- ConvRot256 on the
+ * activations, one INT8 scale per token row, FP16 inputs rotated and
+ * quantised in FP32; the channel pre-scales and SwiGLU are applied before the
+ * rotation, SwiGLU fused into it with no BF16 rounding of its result.  The
+ * SwiGLU itself (gate = first half, value = second half, swish(gate) * value)
+ * is the MLP section of the MiniMax-H3 explainer on modelpad.app.
  *
  *   x       [M][ld_x] in x_dtype (BF16 / FP16 / FP32).  swiglu == 0: columns
  *           0..K-1 are the input.  swiglu != 0: columns 0..K-1 are the gate
@@ -130,9 +143,11 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
                       float* a_scale, cudaStream_t stream);
 
 /*
- * Integer GEMM with the dequantising epilogue (the page's tensor-core INT8
- * GEMM over row-scaled operands; the rescale happens inside the GEMM so no
- * int32 matrix is ever written).
+ * Integer GEMM with the dequantising epilogue.  Source: the NVFP4 loader
+ * entry's GEMM -- an INT8 tensor-core product of the row-scaled operands with
+ * logical N tails and FP16, BF16 or FP32 outputs; the rescale sits inside the
+ * matmul (the MiniMax-H3 explainer's table on moving the rescaling into the
+ * matmul), so no int32 matrix is ever written.
  *
  *   a_q     [M][ld_aq] FP16-stored S8 codes of the rotated activations.
  *   w_q     [N][ld_wq] FP16-stored S8 codes of the rotated weights.
@@ -158,8 +173,9 @@ int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale,
 /*
  * W8A8 with resident weights: widens S8 codes (CONVROT_CODES_S8, e.g. weight
  * codes prepared once and kept at one byte each) into the FP16-held codes
- * that convrot_gemm reads.  The page's W8A8 comparison uses exactly these
- * rotated S8 weights derived from the NVFP4 checkpoint.
+ * that convrot_gemm reads.  Source: the NVFP4 loader entry's W8A8 comparison,
+ * which runs on these same rotated S8 weights derived from the NVFP4
+ * checkpoint.
  *
  *   src  [rows][ld_src] int8, 16-byte aligned, ld_src a multiple of 16.
  *   dst  [rows][ld_dst] FP16, 16-byte aligned, ld_dst a multiple of 8.

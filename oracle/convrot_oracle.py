@@ -4,8 +4,7 @@ TEST INFRASTRUCTURE ONLY: used by tests, the smoke check and the benchmark's
 CPU baseline; never by the product path.  Shares no code with the CUDA side.
 
 What the layer computes (ComfyUI Turing Utils page on comfy.icu, node list,
-entry "Load ConvRot DiT and Load ConvRot CLIP also accept ComfyUI-native
-nvfp4 layers"):
+the entry on the ConvRot DiT / CLIP loaders reading native NVFP4 layers):
 
   1. decode the NVFP4 weight W[n, k] = E2M1(nibble) * E4M3(block scale) *
      FP32 tensor scale for k < K (serialised padding ignored);

@@ -2,8 +2,9 @@
 // dequantising epilogue, and the C-ABI entry points convrot_gemm,
 // convrot_gemm_i32 and convrot_device_error.
 //
-// What it computes (ComfyUI Turing Utils page on comfy.icu, node list, entry
-// "Load ConvRot DiT ... nvfp4": an INT8 tensor-core GEMM over row-scaled
+// What it computes (ComfyUI Turing Utils page on comfy.icu, node list, the
+// entry on the ConvRot loaders reading native NVFP4 layers: an INT8
+// tensor-core GEMM over row-scaled
 // operands, FP16 / BF16 / FP32 outputs, logical N tails; MiniMax-H3
 // explainer on modelpad.app: the rescale lives inside the matmul so the
 // int32 intermediate never touches memory):

@@ -4,11 +4,11 @@
 //   convrot_quant_act:      (SwiGLU ->) (channel pre-scale ->) ConvRot256
 //                           rotation (FP32) -> row S8
 //
-// Both follow the ComfyUI Turing Utils page (comfy.icu), node list, entry
-// "Load ConvRot DiT and Load ConvRot CLIP also accept ComfyUI-native nvfp4
-// layers": paired ConvRot256 on activations and decoded NVFP4 weights, both
-// operands zero-padded to whole 256-blocks, FP32 rotation, row-scaled S8 with
-// a rounded FP32 scale reciprocal; pre-scales and SwiGLU before the rotation.
+// Both follow the ComfyUI Turing Utils page (comfy.icu), node list, the entry
+// on the ConvRot DiT / CLIP loaders reading native NVFP4 layers: paired
+// ConvRot256 on activations and decoded NVFP4 weights, both operands
+// zero-padded to whole 256-blocks, FP32 rotation, row-scaled S8 with a
+// rounded FP32 scale reciprocal; pre-scales and SwiGLU before the rotation.
 // SwiGLU follows the MiniMax-H3 explainer (modelpad.app), MLP section:
 // gate, value = chunk(2); swish(gate) * value.
 #include <cstdint>
@@ -104,17 +104,34 @@ __device__ __forceinline__ void pairs_from_raw(const Raw<DT>& r, float2 (&P)[16]
   for (int b = 0; b < 16; ++b) P[b] = make_float2(raw_elem<DT>(r, b), raw_elem<DT>(r, 16 + b));
 }
 
+// Reciprocal of d in [1, 2] (MUFU, about 1 ulp).  Neither d nor 1/d is ever
+// subnormal here, so flushing subnormals cannot change the result.
+__device__ __forceinline__ float rcp_1to2(float d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+  return r;
+}
+
 // SwiGLU h = g * sigmoid(g) * v in FP32 (no intermediate rounding to the input
-// dtype): h = (g / (1 + exp(-g))) * v.
+// dtype), in a form that never overflows.  With e = exp(-|g|) in (0, 1],
+// sigmoid(g) = 1 / (1 + e) for g >= 0 and e / (1 + e) for g < 0, so
+// h = (g >= 0 ? g : g * e) * (1 / (1 + e)) * v, and the divisor stays in
+// [1, 2].  The direct g / (1 + exp(-g)) divides by an overflowing exp(-g)
+// once g < -88.7, and a fast division returns 0 for divisors above 2^126
+// (g < -87.3) even before that.  e itself is formed as e_h * e_h with
+// e_h = exp(-|g| / 2): g * e_h * e_h stays a normal FP32 number wherever h
+// can still matter (g > -174), also where e alone would be subnormal.
 template <int DT>
 __device__ __forceinline__ void pairs_swiglu(const Raw<DT>& g, const Raw<DT>& v, float2 (&P)[16]) {
 #pragma unroll
   for (int b = 0; b < 16; ++b) {
     const float2 gg = make_float2(raw_elem<DT>(g, b), raw_elem<DT>(g, 16 + b));
     const float2 vv = make_float2(raw_elem<DT>(v, b), raw_elem<DT>(v, 16 + b));
-    // h = (g / (1 + exp(-g))) * v, the two elements of the pair at once
-    const float2 d = add2(make_float2(1.0f, 1.0f), make_float2(expf(-gg.x), expf(-gg.y)));
-    P[b] = mul2(make_float2(__fdividef(gg.x, d.x), __fdividef(gg.y, d.y)), vv);
+    const float2 eh = make_float2(expf(-0.5f * fabsf(gg.x)), expf(-0.5f * fabsf(gg.y)));
+    const float2 gn = mul2(mul2(gg, eh), eh);                       // g * e
+    const float2 num = make_float2(gg.x >= 0.f ? gg.x : gn.x, gg.y >= 0.f ? gg.y : gn.y);
+    const float2 d = add2(make_float2(1.0f, 1.0f), mul2(eh, eh));   // 1 + e
+    P[b] = mul2(mul2(num, make_float2(rcp_1to2(d.x), rcp_1to2(d.y))), vv);
   }
 }
 

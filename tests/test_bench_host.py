@@ -16,9 +16,12 @@ def test_qkv_algorithmic_counts():
     sz = bench.layer_sizes(synth.WORKLOADS["qkv"])
     M, K, N = 19989, 5376, 21504
     assert sz["Kp"] == 5376 and sz["Ks"] == 5376
-    # BF16 input once, FP16 codes once, one FP32 scale per row
+    # algorithmic bytes: BF16 input once, one-byte S8 codes once, one FP32 scale per row
+    assert sz["act_alg"] == M * K * 2 + M * K + 4 * M == 322462548
+    # packed NVFP4 + E4M3 scales once, one-byte codes once, one FP32 scale per row
+    assert sz["w_alg"] == N * K // 2 + N * K // 16 + N * K + 4 * N == 180719616
+    # bytes moved with the codes held as FP16 for the GEMM (and the tensor scale read)
     assert sz["act_bytes"] == M * K * 2 + M * K * 2 + 4 * M == 429923412
-    # packed NVFP4 + E4M3 scales + the tensor scale once, FP16 codes once, one FP32 scale per row
     assert sz["w_bytes"] == N * K // 2 + N * K // 16 + 4 + N * K * 2 + 4 * N == 296325124
     assert sz["gemm_flops"] == 2.0 * M * N * K
     assert abs(sz["gemm_flops"] - 4.6217e12) / 4.6217e12 < 1e-4
@@ -32,6 +35,10 @@ def test_ragged_and_swiglu_counts():
     fd = bench.layer_sizes(synth.WORKLOADS["ffn_down"])
     # the SwiGLU kernel reads gate and value (2K BF16 per token) and writes K codes
     assert fd["act_bytes"] == 19989 * 28672 * 2 + 19989 * 14336 * 2 + 4 * 19989
+    assert fd["act_alg"] == 19989 * 28672 * 2 + 19989 * 14336 + 4 * 19989
+    assert abs(fd["act_alg"] - 1432.9e6) / 1432.9e6 < 1e-3
+    # ragged weights: K_s = 5008 stored, K_p = 5120 codes
+    assert rg["w_alg"] == 21500 * 5008 // 2 + 21500 * 5008 // 16 + 21500 * 5120 + 4 * 21500
 
 
 def test_replica_aggregation():
@@ -48,3 +55,23 @@ def test_source_hash_ignores_comments(tmp_path):
     c.write_text("int f(int x) {\n  return x + 2;\n}\n")
     assert bench.code_sha16(str(a)) == bench.code_sha16(str(b))
     assert bench.code_sha16(str(a)) != bench.code_sha16(str(c))
+
+
+def test_single_gpu_guard_refuses_more_than_one_gpu():
+    bench.single_gpu_guard(1, 1)
+    for n, world in ((2, 1), (1, 2), (8, 8)):
+        with pytest.raises(SystemExit) as e:
+            bench.single_gpu_guard(n, world)
+        assert "one GPU" in str(e.value)
+
+
+def test_tensor_pipe_peak_formula():
+    # 152 SMs at 1920 MHz: 8192 FLOP per clock per SM
+    assert bench.tensor_pipe_peak(152, 1920.0) == pytest.approx(2390.8, rel=1e-4)
+
+
+def test_reference_arm_shares_the_workload_config():
+    wl = synth.WORKLOADS["qkv"]
+    c = bench.bench_config(wl, 0)
+    assert c["workload"] == "qkv M=19989 K=5376 N=21504 bf16->bf16"
+    assert c == bench.bench_config(wl, 0)
