@@ -21,23 +21,27 @@
 // convert each finished chunk to int32 (exact) and add it to per-thread int32
 // registers while the tensor core fills the other buffer.
 //
-// CTA tile 128 x 256 (UMMA M=128, N=256, K=16), K step 64 (one 128-byte
-// swizzled row per operand row), 4-stage TMA ring.  CTAs run in clusters of
-// two that own vertically adjacent M tiles of the same N tile: each CTA
-// loads its own A tile and one half of the shared B tile, multicast into both
-// CTAs, so every SM pulls 32 KiB instead of 48 KiB from L2 per K step.  A
-// stage is refilled only after the MMAs of both CTAs have released it.
-// When the number of M tiles is odd, the last M tile has no partner: its
-// tiles are done "solo", each CTA of a cluster taking its own N tile of that
-// M tile and loading the whole B tile without multicast, so the unpaired row
-// of tiles costs half a pass over N instead of a full one.  Clusters are
-// persistent over a grouped tile order.  Warp 0: TMA producer.
-// Warp 1: TMEM owner and MMA issuer.  Warps 2..9: epilogue, which applies
-// y = fp32(acc) * s_a * s_w (+ bias), stages 32-row x 64-byte boxes in
-// swizzled shared memory and writes them with TMA tensor stores (per-element
-// stores for unaligned outputs).  Every mbarrier wait is bounded: after about
-// two seconds the waiting role records an error code, the CTA drains what it
-// has in flight and returns.
+// Mainloop: the MMA runs on CTA pairs (tcgen05.mma.cta_group::2, M = 256,
+// N = 256, K = 16).  Each CTA of a pair holds its own 128 rows of A and one
+// half (128 columns) of the pair's B tile, so every SM's tensor core reads
+// 32 KiB of shared memory per 64-deep K step instead of 48 KiB, and a stage
+// costs 32 KiB: the ring is 6 stages deep.  Clusters hold two pairs that own
+// the same 256 rows and adjacent N tiles; the two CTAs holding the same 128
+// rows (one in each pair) each load half of those rows and multicast them to
+// both, so a CTA pulls 24 KiB per K step from L2.  The even CTA of a pair
+// issues the MMAs; every load of the pair completes the even CTA's stage
+// barrier.  A stage is refilled only after both pairs' MMAs have released it.
+// An odd number of 256-column N tiles leaves a last column that the two pairs
+// take separately ("solo" work items, A loaded without multicast); an odd
+// number of 128-row M tiles leaves the last pair half empty (its rows past M
+// load as zeros and are not stored).  Clusters are persistent over a grouped
+// tile order.
+// Warp 0: TMA producer.  Warp 1: TMEM owner and (even CTA) MMA issuer.
+// Warps 2..9: epilogue, which applies y = fp32(acc) * s_a * s_w (+ bias),
+// stages 32-row x 64-byte boxes in swizzled shared memory and writes them
+// with TMA tensor stores (per-element stores for unaligned outputs).  Every
+// mbarrier wait is bounded: after about two seconds the waiting role records
+// an error code, the CTA drains what it has in flight and returns.
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -50,18 +54,19 @@
 
 namespace crgemm {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;       // per-CTA output tile 128 x 256; pair tile 256 x 256
+constexpr int STAGES = 6;
 constexpr int KCHUNK_STEPS = 16;                 // 16 * 64 = 1024 K per exact FP32 chunk
-constexpr int A_BYTES = BM * BK * 2;             // 16 KiB
-constexpr int B_BYTES = BN * BK * 2;             // 32 KiB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KiB: this CTA's 128 rows of A
+constexpr int A_HALF_BYTES = A_BYTES / 2;        // 64 rows, the part one CTA loads and multicasts
+constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KiB: this CTA's half (128 columns) of the pair's B
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KiB per CTA
+constexpr int PAIR_STAGE_BYTES = 2 * STAGE_BYTES;// bytes landing in both CTAs of a pair per stage
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32; // 320
 constexpr int TMEM_COLS = 512;                   // two 256-column FP32 buffers
-constexpr int CLUSTER = 2;                       // CTAs sharing one B tile (adjacent M tiles)
-constexpr int B_HALF_BYTES = B_BYTES / CLUSTER;  // part of B each CTA loads and multicasts
-constexpr int GROUP_M = 8;                       // tile raster: 8 M-tile pairs share each B tile
+constexpr int CLUSTER = 4;                       // two CTA pairs: rank = 2 * pair + half
+constexpr int GROUP_M2 = 4;                      // tile raster: 4 pair rows (1024 rows) share each B tile
 // Output staging: each epilogue warp writes its 32 rows x 128 columns as
 // boxes of 32 rows x 64 bytes (64-byte swizzle), two buffers per warp, and
 // hands every box to a TMA tensor store.
@@ -90,10 +95,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -133,23 +134,40 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int cod
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y) {
+// TMA load of one box into this CTA's shared memory at `dst`; its bytes
+// complete the mbarrier at shared::cluster address `bar`, which may lie in
+// the pair's even CTA (.cta_group::2).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
 
-// Same as tma_load_2d, but the tile lands at the same shared-memory offset
-// in every CTA of `mask` and completes the mbarrier at that offset in each.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int x, int y, uint16_t mask) {
+// The same box delivered to the same shared-memory offset in every CTA of
+// `mask`; in each destination the bytes complete the mbarrier at the offset
+// of `bar` in that destination's even (MMA-issuing) CTA, `bar` being an
+// address in an even CTA.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                               uint16_t mask) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;"
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".cta_group::2 [%0], [%1, {%3, %4}], [%2], %5;"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
       : "memory");
+}
+
+// Shared::cluster address of this CTA's shared-memory word `local` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // TMA tensor store of one box from shared memory; completion is tracked
@@ -184,26 +202,25 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(bar) : "memory");
-}
-
 // Arrive on the mbarrier at this offset in every CTA of `mask` once all
-// previously issued tcgen05 operations of this thread have completed.
+// previously issued tcgen05 operations of this thread (pair MMAs) have
+// completed.
 __device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
       ::"r"(bar), "h"(mask) : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, FP16 inputs, FP32 accumulate.
+// Pair MMA: D[tmem] (+)= A * B^T over both CTAs of the pair (M = 256: each
+// CTA's 128 rows of A; N = 256: each CTA's 128 columns of B, at the same
+// shared-memory offsets in both), FP16 inputs, FP32 accumulate; D lands in
+// each CTA's tensor memory for its own 128 rows.
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -242,18 +259,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: D FP32, A and B FP16, both K-major,
-// N = 256, M = 128.
+// N = 256, M = 256 (the pair).
 constexpr uint32_t kIdesc = (1u << 4)                         // D format: F32
                             | (0u << 7) | (0u << 10)          // A, B: F16
                             | (0u << 15) | (0u << 16)         // K-major A and B
                             | (static_cast<uint32_t>(BN >> 3) << 17)
-                            | (static_cast<uint32_t>(BM >> 4) << 24);
+                            | (static_cast<uint32_t>((2 * BM) >> 4) << 24);
 
 struct Params {
   int M, N, K_p;
   int num_m, num_n, k_steps;
-  int num_mp;          // M-tile pairs sharing B tiles (the last M tile is unpaired when num_m is odd)
-  int num_pair_tiles;  // work items of a cluster: num_mp * num_n shared items, then the solo items
+  int num_m2;          // pair rows: 256-row strips (the last one half empty when num_m is odd)
+  int num_shared;      // work items whose two pairs share A: num_m2 * (num_n / 2)
+  int num_items;       // num_shared, then ceil(num_m2 / 2) solo items for the last N tile when num_n is odd
   const float* a_scale;
   const float* w_scale;
   const float* bias;   // optional, [N]
@@ -264,32 +282,27 @@ struct Params {
   int test_stall;   // failure-detection self-test: the producer issues no loads
 };
 
-// Pair tile -> (M-tile pair, N tile), grouped so that GROUP_M pairs in a row
-// reuse each B tile from L2.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& mb, int& nb) {
-  const int per_group = GROUP_M * num_n;
-  const int g = tile / per_group;
-  const int first_m = g * GROUP_M;
-  const int gsize = min(GROUP_M, num_m - first_m);
-  const int r = tile - g * per_group;
-  mb = first_m + r % gsize;
-  nb = r / gsize;
-}
-
-// Work item -> this CTA's (M tile, N tile).  Returns true for a shared item
-// (the pair's M tiles share one B tile, multicast), false for a solo item of
-// the unpaired last M tile (each CTA its own N tile; nb may be past the last
-// N tile for the second CTA, which then computes zeros and stores nothing).
-__device__ __forceinline__ bool work_coords(const Params& p, int item, int rank, int& mb, int& nb) {
-  const int shared_items = p.num_mp * p.num_n;
-  if (item < shared_items) {
-    int mp;
-    tile_coords(item, p.num_mp, p.num_n, mp, nb);
-    mb = mp * CLUSTER + rank;
+// Work item -> this CTA's pair row (256-row strip) and N tile.  Shared items
+// run in a grouped order (GROUP_M2 pair rows in a row reuse each B tile from
+// L2); pair `pair` takes N tile 2 * nb + pair, and both pairs own the same
+// rows, so A is multicast between them.  Solo items cover the last N tile
+// when num_n is odd: the two pairs take pair rows 2 j and 2 j + 1 of it (the
+// second may lie past the last row strip: it then computes zeros and stores
+// nothing).  Returns true for a shared item.
+__device__ __forceinline__ bool work_coords(const Params& p, int item, int pair, int& m2, int& nt) {
+  if (item < p.num_shared) {
+    const int n2 = p.num_n >> 1;
+    const int per_group = GROUP_M2 * n2;
+    const int g = item / per_group;
+    const int first = g * GROUP_M2;
+    const int gsize = min(GROUP_M2, p.num_m2 - first);
+    const int r = item - g * per_group;
+    m2 = first + r % gsize;
+    nt = 2 * (r / gsize) + pair;
     return true;
   }
-  mb = p.num_m - 1;
-  nb = (item - shared_items) * CLUSTER + rank;
+  m2 = 2 * (item - p.num_shared) + pair;
+  nt = p.num_n - 1;
   return false;
 }
 
@@ -318,7 +331,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + OUT_STAGING);
-  // barrier slots: full[4], empty[4], acc_full[2], acc_empty[2], drain
+  // barrier slots: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
@@ -326,15 +339,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const uint32_t half = rank & 1u, pair = rank >> 1;     // half: which 128 rows of the pair's 256
+  const uint32_t leader = rank & ~1u;                     // the pair's even CTA: issues the MMAs
+  const bool is_leader = half == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CLUSTER);      // released by the MMAs of both CTAs
+      mbar_init(full0 + 8 * s, 1);               // the even CTA's producer + PAIR_STAGE_BYTES of loads
+      mbar_init(empty0 + 8 * s, 2);              // released by the MMAs of both pairs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
-      mbar_init(acce0 + 8 * b, NUM_EPI_WARPS);
+      mbar_init(acce0 + 8 * b, 2 * NUM_EPI_WARPS);   // epilogue warps of both CTAs of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -346,65 +363,69 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+    // one warp of each CTA of the pair allocates the same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(const_cast<uint32_t*>(tmem_slot))), "r"(TMEM_COLS) : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
-  // the peer's multicasts and commits target our barriers: both CTAs must
-  // have initialised theirs before either issues anything
+  // other CTAs' loads, multicasts and commits target our barriers: every CTA
+  // of the cluster must have initialised its barriers before any is issued
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int rank = static_cast<int>(cluster_rank());
   const int cluster_id = blockIdx.x / CLUSTER, num_clusters = gridDim.x / CLUSTER;
-  constexpr uint16_t kPeers = (1u << CLUSTER) - 1u;
+  constexpr uint16_t kAll = (1u << CLUSTER) - 1u;
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pair));
+  const uint16_t a_mask = static_cast<uint16_t>((1u << half) | (1u << (half + 2)));   // same rows, both pairs
 
   const int k_steps = p.k_steps;
   const int chunks_per_tile = (k_steps + KCHUNK_STEPS - 1) / KCHUNK_STEPS;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      uint32_t issued_mask = 0, issued_phase = 0;   // last outstanding load per stage
-      for (int tile = cluster_id; tile < p.num_pair_tiles && ok && !p.test_stall; tile += num_clusters) {
-        int mb, nb;
-        const bool shared_b = work_coords(p, tile, rank, mb, nb);
+      uint32_t issued_mask = 0, issued_phase = 0;   // even CTA: last outstanding stage phase
+      const uint32_t lfull0 = map_to_rank(full0, leader);
+      for (int tile = cluster_id; tile < p.num_items && ok && !p.test_stall; tile += num_clusters) {
+        int m2, nt;
+        const bool shared_a = work_coords(p, tile, static_cast<int>(pair), m2, nt);
+        const int m_row = (2 * m2 + static_cast<int>(half)) * BM;
         for (int ks = 0; ks < k_steps; ++ks) {
-          // the stage is free once the MMAs of BOTH CTAs have consumed it
+          // the stage is free once the MMAs of BOTH pairs have consumed it
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, ERR_WAIT_EMPTY, abort_flag)) { ok = false; break; }
-          const uint32_t fb = full0 + 8 * stage;
-          // own A tile + both halves of B: ours and the peer's multicast, or
-          // (solo item) both halves of our own B tile
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t fb = lfull0 + 8 * stage;
+          if (is_leader) mbar_arrive_expect_tx(full0 + 8 * stage, PAIR_STAGE_BYTES);
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          tma_load_2d(sa, &tmap_a, fb, ks * BK, mb * BM);
-          if (shared_b) {
-            tma_load_2d_mc(sa + A_BYTES + rank * B_HALF_BYTES, &tmap_b, fb, ks * BK,
-                           nb * BN + rank * (BN / CLUSTER), kPeers);
+          if (shared_a) {
+            // our half of the 128 rows, into this CTA and the same-rows CTA of the other pair
+            tma_load_2d_mc(sa + pair * A_HALF_BYTES, &tmap_a, fb, ks * BK, m_row + static_cast<int>(pair) * (BM / 2),
+                           a_mask);
           } else {
 #pragma unroll
-            for (int h = 0; h < CLUSTER; ++h)
-              tma_load_2d(sa + A_BYTES + h * B_HALF_BYTES, &tmap_b, fb, ks * BK, nb * BN + h * (BN / CLUSTER));
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sa + h * A_HALF_BYTES, &tmap_a, fb, ks * BK, m_row + h * (BM / 2));
           }
+          tma_load_2d(sa + A_BYTES, &tmap_b, fb, ks * BK, nt * BN + static_cast<int>(half) * (BN / 2));
           issued_mask |= 1u << stage;
           issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       if (ok) {
-        // the peer's MMA commits arrive on our empty barriers: wait until both
-        // CTAs have released the last use of every stage before leaving
+        // the other CTAs' MMA commits arrive on our empty barriers: wait until
+        // both pairs have released the last use of every stage before leaving
         for (int i = 0; i < STAGES; ++i) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, ERR_WAIT_EMPTY, abort_flag)) break;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-      } else {
-        // let every load still in flight land before the CTA can exit
+      } else if (is_leader) {
+        // let every load still in flight into the pair land before the CTAs
+        // can exit (the even CTA's barriers count the whole pair's bytes)
         for (int s = 0; s < STAGES; ++s)
           if (issued_mask & (1u << s)) {
             const uint64_t t0 = globaltimer();
@@ -414,14 +435,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    if (lane == 0 && is_leader) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t chunk = 0;          // running chunk counter -> TMEM buffer and its phase
       bool ok = true;
       bool any = false;
-      for (int tile = cluster_id; tile < p.num_pair_tiles && ok; tile += num_clusters) {
+      for (int tile = cluster_id; tile < p.num_items && ok; tile += num_clusters) {
         for (int c = 0; c < chunks_per_tile && ok; ++c, ++chunk) {
           const uint32_t buf = chunk & 1u, use = chunk >> 1;
           if (!mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, ERR_WAIT_ACC_EMPTY, abort_flag)) { ok = false; break; }
@@ -439,15 +460,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
               tc_mma_f16(d_tmem, da + 2 * kk, db + 2 * kk, kIdesc, (ks > ks0 || kk > 0) ? 1u : 0u);
             }
             any = true;
-            tc_commit_mc(empty0 + 8 * stage, kPeers);
+            tc_commit_mc(empty0 + 8 * stage, kAll);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
-          if (ok) tc_commit(accf0 + 8 * buf);
+          if (ok) tc_commit_mc(accf0 + 8 * buf, pair_mask);
         }
       }
       if (!ok && any) {
-        // wait for the tensor core to finish everything issued before TMEM is freed
-        tc_commit(drain);
+        // wait for the tensor cores to finish everything issued before TMEM is freed
+        tc_commit_mc(drain, static_cast<uint16_t>(1u << rank));
         const uint64_t t0 = globaltimer();
         while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitLimitNs) {}
       }
@@ -461,9 +482,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     uint32_t chunk = 0;
     uint32_t boxes = 0;                       // output boxes staged by this warp so far
     bool ok = true;
-    for (int tile = cluster_id; tile < p.num_pair_tiles && ok; tile += num_clusters) {
-      int mb, nb;
-      work_coords(p, tile, rank, mb, nb);
+    const uint32_t lacce0 = map_to_rank(acce0, leader);   // the even CTA's acc_empty barriers
+    for (int tile = cluster_id; tile < p.num_items && ok; tile += num_clusters) {
+      int m2, nt;
+      work_coords(p, tile, static_cast<int>(pair), m2, nt);
+      const int mb = 2 * m2 + static_cast<int>(half), nb = nt;
       int32_t acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0;
@@ -489,7 +512,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+        if (lane == 0) mbar_arrive_cluster(lacce0 + 8 * buf);
       }
       if (!ok) break;
       // ---- output: this thread owns row m, columns n0 .. n0+127
@@ -592,10 +615,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();            // neither CTA leaves while its peer may still write into it
+  cluster_sync();            // no CTA leaves while another may still write into it
   tc_fence_after();
   if (warp == 1) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
                  : "memory");
   }
 }
@@ -654,7 +677,7 @@ static bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int
 }
 
 // Persistent grid: as many clusters as can be resident at once (one CTA per
-// SM), never more than there are pair tiles.
+// SM), never more than there are work items.
 template <int OUT, bool BIAS, bool TMA_OUT>
 static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mo,
                           const Params& p, cudaStream_t st) {
@@ -692,7 +715,7 @@ static cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, const CU
     }
     max_clusters = n;
   }
-  const int clusters = p.num_pair_tiles < max_clusters ? p.num_pair_tiles : max_clusters;
+  const int clusters = p.num_items < max_clusters ? p.num_items : max_clusters;
   cfg.gridDim = dim3(clusters * CLUSTER);
   return cudaLaunchKernelEx(&cfg, gemm_kernel<OUT, BIAS, TMA_OUT>, ma, mb, mo, p);
 }
@@ -728,8 +751,9 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.K_p = K_p;
   p.num_m = (M + BM - 1) / BM;
   p.num_n = (N + BN - 1) / BN;
-  p.num_mp = p.num_m / CLUSTER;
-  p.num_pair_tiles = p.num_mp * p.num_n + (p.num_m % CLUSTER ? (p.num_n + CLUSTER - 1) / CLUSTER : 0);
+  p.num_m2 = (p.num_m + 1) / 2;
+  p.num_shared = p.num_m2 * (p.num_n / 2);
+  p.num_items = p.num_shared + (p.num_n % 2 ? (p.num_m2 + 1) / 2 : 0);
   p.k_steps = K_p / BK;
   p.a_scale = a_scale;
   p.w_scale = w_scale;
@@ -737,7 +761,7 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.ld_out = ld_out;
   p.out_vec = (reinterpret_cast<uintptr_t>(out) % 16 == 0) && ((ld_out * static_cast<int64_t>(out_esize)) % 16 == 0);
   CUtensorMap ma, mb;
-  if (!make_map(&ma, a_q, M, K_p, ld_aq, BM) || !make_map(&mb, w_q, N, K_p, ld_wq, BN / CLUSTER))
+  if (!make_map(&ma, a_q, M, K_p, ld_aq, BM / 2) || !make_map(&mb, w_q, N, K_p, ld_wq, BN / 2))
     return convrot::record_error("cuTensorMapEncodeTiled failed for an operand map");
   CUtensorMap mo;
   memset(&mo, 0, sizeof(mo));
