@@ -24,18 +24,18 @@
 // Mainloop: the MMA runs on CTA pairs (tcgen05.mma.cta_group::2, M = 256,
 // N = 256, K = 16).  Each CTA of a pair holds its own 128 rows of A and one
 // half (128 columns) of the pair's B tile, so every SM's tensor core reads
-// 32 KiB of shared memory per 64-deep K step instead of 48 KiB, and a stage
-// costs 32 KiB: the ring is 6 stages deep.  Clusters hold two pairs that own
-// the same 256 rows and adjacent N tiles; the two CTAs holding the same 128
-// rows (one in each pair) each load half of those rows and multicast them to
-// both, so a CTA pulls 24 KiB per K step from L2.  The even CTA of a pair
-// issues the MMAs; every load of the pair completes the even CTA's stage
-// barrier.  A stage is refilled only after both pairs' MMAs have released it.
-// An odd number of 256-column N tiles leaves a last column that the two pairs
-// take separately ("solo" work items, A loaded without multicast); an odd
-// number of 128-row M tiles leaves the last pair half empty (its rows past M
-// load as zeros and are not stored).  Clusters are persistent over a grouped
-// tile order.
+// 32 KiB of shared memory per 64-deep K step instead of the 48 KiB of a
+// one-CTA 128 x 256 tile, and a stage costs 32 KiB: the ring is 6 stages
+// deep.  The even CTA of a pair issues the MMAs; every load of the pair
+// completes the even CTA's stage barrier.  A cluster is one pair (NPAIRS = 1):
+// 76 clusters fill the 152 SMs.  With two pairs per cluster (NPAIRS = 2) the
+// pairs share A by multicast, which saves a quarter of the L2 reads, but only
+// 36 four-CTA clusters fit at once, 144 SMs, and it measured 3-8% slower.
+// With two pairs, an odd number of 256-column N tiles leaves a last column
+// that the pairs take separately ("solo" work items).  An odd number of
+// 128-row M tiles leaves the last pair half empty (its rows past M load as
+// zeros and are not stored).  Clusters are persistent over a grouped tile
+// order.
 // Warp 0: TMA producer.  Warp 1: TMEM owner and (even CTA) MMA issuer.
 // Warps 2..9: epilogue, which applies y = fp32(acc) * s_a * s_w (+ bias),
 // stages 32-row x 64-byte boxes in swizzled shared memory and writes them
@@ -65,14 +65,16 @@ constexpr int PAIR_STAGE_BYTES = 2 * STAGE_BYTES;// bytes landing in both CTAs o
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int THREADS = 64 + NUM_EPI_WARPS * 32; // 320
 constexpr int TMEM_COLS = 512;                   // two 256-column FP32 buffers
-constexpr int CLUSTER = 4;                       // two CTA pairs: rank = 2 * pair + half
-constexpr int GROUP_M2 = 4;                      // tile raster: 4 pair rows (1024 rows) share each B tile
+constexpr int NPAIRS = 1;                        // CTA pairs per cluster (2: they share A by multicast)
+constexpr int CLUSTER = 2 * NPAIRS;              // rank = 2 * pair + half
+constexpr int GROUP_M2 = 8;                      // tile raster: 8 pair rows (2048 rows) share each B tile
 // Output staging: each epilogue warp writes its 32 rows x 128 columns as
-// boxes of 32 rows x 64 bytes (64-byte swizzle), two buffers per warp, and
-// hands every box to a TMA tensor store.
+// boxes of 32 rows x 64 bytes (64-byte swizzle), OUT_BUFS buffers per warp,
+// and hands every box to a TMA tensor store.
 constexpr int OUT_BOX_BYTES = 64;
 constexpr int OUT_BOX = 32 * OUT_BOX_BYTES;                  // 2 KiB
-constexpr int OUT_STAGING = NUM_EPI_WARPS * 2 * OUT_BOX;     // 32 KiB
+constexpr int OUT_BUFS = 2;
+constexpr int OUT_STAGING = NUM_EPI_WARPS * OUT_BUFS * OUT_BOX;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -165,9 +167,13 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
   return r;
 }
 
-// Arrive (release, cluster scope) on an mbarrier given by its shared::cluster address.
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
+// another's), with the default CTA-scope release: the epilogue uses it to
+// hand a drained TMEM buffer back to the pair's MMA issuer, and the tensor
+// memory reads it orders are fenced by tcgen05.fence::before_thread_sync (a
+// cluster-scope release here made every arrive a cluster-wide memory fence).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // TMA tensor store of one box from shared memory; completion is tracked
@@ -177,7 +183,9 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sr
                ::"l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(x), "r"(y) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Wait until at most N of this thread's bulk store groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -290,6 +298,16 @@ struct Params {
 // second may lie past the last row strip: it then computes zeros and stores
 // nothing).  Returns true for a shared item.
 __device__ __forceinline__ bool work_coords(const Params& p, int item, int pair, int& m2, int& nt) {
+  if (NPAIRS == 1) {              // one pair per cluster: items are (pair row, N tile)
+    const int per_group = GROUP_M2 * p.num_n;
+    const int g = item / per_group;
+    const int first = g * GROUP_M2;
+    const int gsize = min(GROUP_M2, p.num_m2 - first);
+    const int r = item - g * per_group;
+    m2 = first + r % gsize;
+    nt = r / gsize;
+    return false;
+  }
   if (item < p.num_shared) {
     const int n2 = p.num_n >> 1;
     const int per_group = GROUP_M2 * n2;
@@ -319,6 +337,19 @@ template <> __device__ __forceinline__ __nv_bfloat16 to_out<CONVROT_BF16>(float 
 template <> __device__ __forceinline__ __half to_out<CONVROT_FP16>(float y) { return __float2half_rn(y); }
 template <> __device__ __forceinline__ float to_out<CONVROT_FP32>(float y) { return y; }
 
+// Two outputs rounded (nearest even, each on its own) into one 32-bit word,
+// the first in the low half: one packed conversion instead of two.
+template <int OUT>
+__device__ __forceinline__ uint32_t to_out2(float y0, float y1);
+template <> __device__ __forceinline__ uint32_t to_out2<CONVROT_BF16>(float y0, float y1) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <> __device__ __forceinline__ uint32_t to_out2<CONVROT_FP16>(float y0, float y1) {
+  const __half2 h = __floats2half2_rn(y0, y1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // OUT = CONVROT_BF16 / FP16 / FP32, or -1 for raw int32 accumulators.
 // BIAS: p.bias is non-null and added in the epilogue.
 // TMA_OUT: staged output boxes go out by TMA tensor stores (output base and
@@ -347,7 +378,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);               // the even CTA's producer + PAIR_STAGE_BYTES of loads
-      mbar_init(empty0 + 8 * s, 2);              // released by the MMAs of both pairs
+      mbar_init(empty0 + 8 * s, NPAIRS);         // released by the MMAs of every pair
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
@@ -378,10 +409,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   const int cluster_id = blockIdx.x / CLUSTER, num_clusters = gridDim.x / CLUSTER;
   constexpr uint16_t kAll = (1u << CLUSTER) - 1u;
   const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pair));
-  const uint16_t a_mask = static_cast<uint16_t>((1u << half) | (1u << (half + 2)));   // same rows, both pairs
+  const uint16_t a_mask = static_cast<uint16_t>(NPAIRS == 2 ? (1u << half) | (1u << (half + 2)) : 0u);
 
   const int k_steps = p.k_steps;
+  // K steps are split into equal chunks of at most KCHUNK_STEPS: a short last
+  // chunk would leave the epilogue less time to drain the buffer it follows
+  // (K = 5376: six chunks of 896 instead of five of 1024 and one of 256)
   const int chunks_per_tile = (k_steps + KCHUNK_STEPS - 1) / KCHUNK_STEPS;
+  const int chunk_steps = (k_steps + chunks_per_tile - 1) / chunks_per_tile;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
@@ -448,7 +483,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           if (!mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, ERR_WAIT_ACC_EMPTY, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
-          const int ks0 = c * KCHUNK_STEPS, ks1 = min(k_steps, ks0 + KCHUNK_STEPS);
+          const int ks0 = c * chunk_steps, ks1 = min(k_steps, ks0 + chunk_steps);
           for (int ks = ks0; ks < ks1; ++ks) {
             if (!mbar_wait(full0 + 8 * stage, phase, ERR_WAIT_FULL, abort_flag)) { ok = false; break; }
             tc_fence_after();
@@ -535,13 +570,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
           // base or pitch not 16-byte aligned) by the warp with element
           // stores that walk each row: consecutive lanes, consecutive columns
           constexpr int CPB = OUT_BOX_BYTES / sizeof(T);   // columns per box
-          uint8_t* wstage = staging + ew * 2 * OUT_BOX;
+          uint8_t* wstage = staging + ew * OUT_BUFS * OUT_BOX;
 #pragma unroll
           for (int b = 0; b < 128 / CPB; ++b) {
-            const int buf = static_cast<int>(boxes & 1u);
-            if (boxes >= 2) {
-              // the store issued from this buffer two boxes ago must have read it
-              if (lane == 0) bulk_wait_read_1();
+            const int buf = static_cast<int>(boxes % OUT_BUFS);
+            if (boxes >= OUT_BUFS) {
+              // the store issued from this buffer OUT_BUFS boxes ago must have read it
+              if (lane == 0) bulk_wait_read<OUT_BUFS - 1>();
               __syncwarp();
             }
             ++boxes;
@@ -570,11 +605,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                   bs[q] = (BIAS && n + q < p.N) ? __ldg(p.bias + n + q) : 0.f;
                 }
               }
-              union { T v[VEC]; uint4 u; } pk;
+              union { T v[VEC]; uint32_t w[4]; uint4 u; } pk;
+              float yv[VEC];
 #pragma unroll
               for (int q = 0; q < VEC; ++q) {
                 const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + q]), sa), sw[q]);
-                pk.v[q] = to_out<OUT>(BIAS ? __fadd_rn(y, bs[q]) : y);
+                yv[q] = BIAS ? __fadd_rn(y, bs[q]) : y;
+              }
+              if constexpr (sizeof(T) == 2) {
+#pragma unroll
+                for (int q = 0; q < VEC; q += 2) pk.w[q / 2] = to_out2<OUT>(yv[q], yv[q + 1]);
+              } else {
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) pk.v[q] = to_out<OUT>(yv[q]);
               }
               // 64-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ ((r >> 1) & 3)
               *reinterpret_cast<uint4*>(rowp + ((c ^ ((lane >> 1) & 3)) << 4)) = pk.u;
@@ -752,8 +795,13 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.num_m = (M + BM - 1) / BM;
   p.num_n = (N + BN - 1) / BN;
   p.num_m2 = (p.num_m + 1) / 2;
-  p.num_shared = p.num_m2 * (p.num_n / 2);
-  p.num_items = p.num_shared + (p.num_n % 2 ? (p.num_m2 + 1) / 2 : 0);
+  if (NPAIRS == 2) {
+    p.num_shared = p.num_m2 * (p.num_n / 2);
+    p.num_items = p.num_shared + (p.num_n % 2 ? (p.num_m2 + 1) / 2 : 0);
+  } else {
+    p.num_shared = 0;
+    p.num_items = p.num_m2 * p.num_n;
+  }
   p.k_steps = K_p / BK;
   p.a_scale = a_scale;
   p.w_scale = w_scale;
