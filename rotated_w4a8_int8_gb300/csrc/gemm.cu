@@ -233,18 +233,14 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
-// row (lane base + i), columns col .. col+31.
-__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+// 32 lanes x 16 consecutive 32-bit columns (thread i: row lane base + i).
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 
@@ -534,15 +530,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         if (!got) { ok = false; break; }
         tc_fence_after();
         const uint32_t t_base = tmem_base + lane_addr + buf * BN + col_half * 128;
+        // 16 columns per load: with 32, the 128 int32 accumulators and the
+        // load's registers exceed the 168-register budget and spill
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_base + g * 32, r);
+        for (int g = 0; g < 8; ++g) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(t_base + g * 16, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 16; ++j) {
             // the FP32 value is an exact integer below 2^24: conversion is exact
-            acc[g * 32 + j] += __float2int_rn(__uint_as_float(r[j]));
+            acc[g * 16 + j] += __float2int_rn(__uint_as_float(r[j]));
           }
         }
         tc_fence_before();
