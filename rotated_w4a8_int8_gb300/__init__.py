@@ -87,6 +87,15 @@ def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
+def _ld(t) -> int:
+    """Row pitch in elements.  Torch may report any stride (often 0) for a
+    dimension of size 1; a single row has no pitch, so its own width is
+    passed instead (rows must be contiguous)."""
+    if t.dim() >= 2 and t.shape[0] <= 1:
+        return max(int(t.stride(0)), int(t.shape[1]))
+    return int(t.stride(0))
+
+
 def _stream(stream) -> int:
     if stream is None:
         import torch
@@ -115,7 +124,7 @@ def prepare_weight(w_fp4, w_sf, w_tensor_scale, K: int, w_q, w_scale, stream=Non
     N = w_fp4.shape[0]
     _check("convrot_prepare_weight", load_library().convrot_prepare_weight(
         _ptr(w_fp4), _ptr(w_sf), _ptr(w_tensor_scale), N, int(K), _ptr(w_q), _codes_fmt(w_q),
-        w_q.stride(0), _ptr(w_scale), _stream(stream)))
+        _ld(w_q), _ptr(w_scale), _stream(stream)))
 
 
 def quant_act(x, K: int, a_q, a_scale, swiglu: bool = False, pre_scale=None, stream=None) -> None:
@@ -123,8 +132,8 @@ def quant_act(x, K: int, a_q, a_scale, swiglu: bool = False, pre_scale=None, str
     [M, >=K_p], a_scale float32 [M], pre_scale None or float32 [K]."""
     M = x.shape[0]
     _check("convrot_quant_act", load_library().convrot_quant_act(
-        _ptr(x), _dtype_code(x), x.stride(0), M, int(K), int(bool(swiglu)), _ptr(pre_scale),
-        _ptr(a_q), _codes_fmt(a_q), a_q.stride(0), _ptr(a_scale), _stream(stream)))
+        _ptr(x), _dtype_code(x), _ld(x), M, int(K), int(bool(swiglu)), _ptr(pre_scale),
+        _ptr(a_q), _codes_fmt(a_q), _ld(a_q), _ptr(a_scale), _stream(stream)))
 
 
 def gemm(a_q, a_scale, w_q, w_scale, out, K_p: int | None = None, bias=None, stream=None) -> None:
@@ -133,8 +142,8 @@ def gemm(a_q, a_scale, w_q, w_scale, out, K_p: int | None = None, bias=None, str
     M, N = a_q.shape[0], w_q.shape[0]
     K_p = a_q.shape[1] if K_p is None else K_p
     _check("convrot_gemm", load_library().convrot_gemm(
-        _ptr(a_q), a_q.stride(0), _ptr(a_scale), _ptr(w_q), w_q.stride(0), _ptr(w_scale),
-        _ptr(bias), M, N, int(K_p), _ptr(out), _dtype_code(out), out.stride(0), _stream(stream)))
+        _ptr(a_q), _ld(a_q), _ptr(a_scale), _ptr(w_q), _ld(w_q), _ptr(w_scale),
+        _ptr(bias), M, N, int(K_p), _ptr(out), _dtype_code(out), _ld(out), _stream(stream)))
 
 
 def gemm_i32(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:
@@ -142,8 +151,8 @@ def gemm_i32(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:
     M, N = a_q.shape[0], w_q.shape[0]
     K_p = a_q.shape[1] if K_p is None else K_p
     _check("convrot_gemm_i32", load_library().convrot_gemm_i32(
-        _ptr(a_q), a_q.stride(0), _ptr(w_q), w_q.stride(0), M, N, int(K_p), _ptr(acc),
-        acc.stride(0), _stream(stream)))
+        _ptr(a_q), _ld(a_q), _ptr(w_q), _ld(w_q), M, N, int(K_p), _ptr(acc),
+        _ld(acc), _stream(stream)))
 
 
 def widen_codes(src, dst, cols: int | None = None, stream=None) -> None:
@@ -151,7 +160,7 @@ def widen_codes(src, dst, cols: int | None = None, stream=None) -> None:
     rows = src.shape[0]
     cols = src.shape[1] if cols is None else cols
     _check("convrot_widen_codes", load_library().convrot_widen_codes(
-        _ptr(src), src.stride(0), rows, int(cols), _ptr(dst), dst.stride(0), _stream(stream)))
+        _ptr(src), _ld(src), rows, int(cols), _ptr(dst), _ld(dst), _stream(stream)))
 
 
 def gemm_timeout_selftest(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:
@@ -159,8 +168,8 @@ def gemm_timeout_selftest(a_q, w_q, acc, K_p: int | None = None, stream=None) ->
     M, N = a_q.shape[0], w_q.shape[0]
     K_p = a_q.shape[1] if K_p is None else K_p
     _check("convrot_gemm_timeout_selftest", load_library().convrot_gemm_timeout_selftest(
-        _ptr(a_q), a_q.stride(0), _ptr(w_q), w_q.stride(0), M, N, int(K_p), _ptr(acc),
-        acc.stride(0), _stream(stream)))
+        _ptr(a_q), _ld(a_q), _ptr(w_q), _ld(w_q), M, N, int(K_p), _ptr(acc),
+        _ld(acc), _stream(stream)))
 
 
 def device_error(stream=None) -> int:

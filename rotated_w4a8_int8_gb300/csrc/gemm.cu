@@ -67,6 +67,7 @@ constexpr int THREADS = 64 + NUM_EPI_WARPS * 32; // 320
 constexpr int TMEM_COLS = 512;                   // two 256-column FP32 buffers
 constexpr int NPAIRS = 1;                        // CTA pairs per cluster (2: they share A by multicast)
 constexpr int CLUSTER = 2 * NPAIRS;              // rank = 2 * pair + half
+constexpr int A_BOX_ROWS = NPAIRS == 2 ? BM / 2 : BM;   // rows of A per TMA load (halves when multicast)
 constexpr int GROUP_M2 = 8;                      // tile raster: 8 pair rows (2048 rows) share each B tile
 // Output staging: each epilogue warp writes its 32 rows x 128 columns as
 // boxes of 32 rows x 64 bytes (64-byte swizzle), OUT_BUFS buffers per warp,
@@ -438,8 +439,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
                            a_mask);
           } else {
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_2d(sa + h * A_HALF_BYTES, &tmap_a, fb, ks * BK, m_row + h * (BM / 2));
+            for (int h = 0; h < BM / A_BOX_ROWS; ++h)
+              tma_load_2d(sa + h * (A_BOX_ROWS * BK * 2), &tmap_a, fb, ks * BK, m_row + h * A_BOX_ROWS);
           }
           tma_load_2d(sa + A_BYTES, &tmap_b, fb, ks * BK, nt * BN + static_cast<int>(half) * (BN / 2));
           issued_mask |= 1u << stage;
@@ -807,7 +808,7 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
   p.ld_out = ld_out;
   p.out_vec = (reinterpret_cast<uintptr_t>(out) % 16 == 0) && ((ld_out * static_cast<int64_t>(out_esize)) % 16 == 0);
   CUtensorMap ma, mb;
-  if (!make_map(&ma, a_q, M, K_p, ld_aq, BM / 2) || !make_map(&mb, w_q, N, K_p, ld_wq, BN / 2))
+  if (!make_map(&ma, a_q, M, K_p, ld_aq, A_BOX_ROWS) || !make_map(&mb, w_q, N, K_p, ld_wq, BN / 2))
     return convrot::record_error("cuTensorMapEncodeTiled failed for an operand map");
   CUtensorMap mo;
   memset(&mo, 0, sizeof(mo));

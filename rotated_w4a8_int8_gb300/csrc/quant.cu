@@ -118,19 +118,18 @@ __device__ __forceinline__ float rcp_1to2(float d) {
 // h = (g >= 0 ? g : g * e) * (1 / (1 + e)) * v, and the divisor stays in
 // [1, 2].  The direct g / (1 + exp(-g)) divides by an overflowing exp(-g)
 // once g < -88.7, and a fast division returns 0 for divisors above 2^126
-// (g < -87.3) even before that.  e itself is formed as e_h * e_h with
-// e_h = exp(-|g| / 2): g * e_h * e_h stays a normal FP32 number wherever h
-// can still matter (g > -174), also where e alone would be subnormal.
+// (g < -87.3) even before that, where h is still a normal FP32 number.
+// Below g = -87.3, e is subnormal and g * e stays normal down to g = -92.
 template <int DT>
 __device__ __forceinline__ void pairs_swiglu(const Raw<DT>& g, const Raw<DT>& v, float2 (&P)[16]) {
 #pragma unroll
   for (int b = 0; b < 16; ++b) {
     const float2 gg = make_float2(raw_elem<DT>(g, b), raw_elem<DT>(g, 16 + b));
     const float2 vv = make_float2(raw_elem<DT>(v, b), raw_elem<DT>(v, 16 + b));
-    const float2 eh = make_float2(expf(-0.5f * fabsf(gg.x)), expf(-0.5f * fabsf(gg.y)));
-    const float2 gn = mul2(mul2(gg, eh), eh);                       // g * e
-    const float2 num = make_float2(gg.x >= 0.f ? gg.x : gn.x, gg.y >= 0.f ? gg.y : gn.y);
-    const float2 d = add2(make_float2(1.0f, 1.0f), mul2(eh, eh));   // 1 + e
+    const float2 e = make_float2(expf(-fabsf(gg.x)), expf(-fabsf(gg.y)));
+    const float2 ge = mul2(gg, e);
+    const float2 num = make_float2(gg.x >= 0.f ? gg.x : ge.x, gg.y >= 0.f ? gg.y : ge.y);
+    const float2 d = add2(make_float2(1.0f, 1.0f), e);
     P[b] = mul2(mul2(num, make_float2(rcp_1to2(d.x), rcp_1to2(d.y))), vv);
   }
 }

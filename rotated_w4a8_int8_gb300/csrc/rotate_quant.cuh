@@ -278,6 +278,22 @@ __device__ __forceinline__ uint32_t code_byte(float v) {
   else return static_cast<uint32_t>(__float2int_rn(v)) & 0xffu;
 }
 
+// FP16 codes of two values (already multiplied by r) without the conversion
+// pipe.  kF16Magic = 1.5 * 2^23 + 0x6600 is an even integer in [2^23, 2^24),
+// where the FP32 spacing is 1, so fp32(v + kF16Magic) = kF16Magic + rint(v)
+// (half to even, as kF16Magic is even) for |v| < 2^21; its bit pattern is
+// 0x4B406600 + code, whose low 16 bits 0x6600 + code (code in [-127, 127])
+// are the FP16 encoding of 1536 + code.  One byte permute gathers the two
+// low halves, and an exact FP16 subtraction of 1536 leaves the two codes.
+constexpr float kF16Magic = 12609024.0f;
+
+__device__ __forceinline__ __half2 f16_code_pair(float v0, float v1) {
+  const uint32_t b0 = __float_as_uint(__fadd_rn(v0, kF16Magic));
+  const uint32_t b1 = __float_as_uint(__fadd_rn(v1, kF16Magic));
+  const uint32_t w = __byte_perm(b0, b1, 0x5410);
+  return __hsub2(*reinterpret_cast<const __half2*>(&w), __float2half2_rn(1536.0f));
+}
+
 // Writes the codes of one block: values (already multiplied by r, so only
 // the rounding is left) for rows 2p, 2p+1 and columns 2q, 2q+1.
 template <bool MAGIC>
@@ -288,8 +304,13 @@ __device__ __forceinline__ void store_codes(void* q_row, bool f16_codes, int blk
     __half2* q = reinterpret_cast<__half2*>(static_cast<__half*>(q_row) + col);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-      q[(32 * p) / 2] = __floats2half2_rn(rint_f<MAGIC>(c.U[p].x), rint_f<MAGIC>(c.V[p].x));        // row 2p
-      q[(32 * p + 16) / 2] = __floats2half2_rn(rint_f<MAGIC>(c.U[p].y), rint_f<MAGIC>(c.V[p].y));   // row 2p+1
+      if constexpr (MAGIC) {
+        q[(32 * p) / 2] = f16_code_pair(c.U[p].x, c.V[p].x);                                       // row 2p
+        q[(32 * p + 16) / 2] = f16_code_pair(c.U[p].y, c.V[p].y);                                  // row 2p+1
+      } else {
+        q[(32 * p) / 2] = __floats2half2_rn(rint_f<false>(c.U[p].x), rint_f<false>(c.V[p].x));     // row 2p
+        q[(32 * p + 16) / 2] = __floats2half2_rn(rint_f<false>(c.U[p].y), rint_f<false>(c.V[p].y));
+      }
     }
   } else {
     uint16_t* q = reinterpret_cast<uint16_t*>(static_cast<int8_t*>(q_row) + col);

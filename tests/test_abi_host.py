@@ -116,3 +116,14 @@ def test_widen_codes_rejects_bad_arguments(lib):
     assert f(P, 64, 4, 48, P, 60, 0) == 2           # ld_dst not a multiple of 8
     assert f(None, 64, 4, 48, P, 64, 0) == 1
     assert f(P, 64, 0, 48, P, 64, 0) == 0           # empty
+
+
+def test_single_row_tensors_pass_their_width_as_pitch():
+    # torch reports stride 0 for a leading dimension of size 1 (e.g. a numpy
+    # view with a new axis); the binding passes the row width instead
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(np.zeros(512)[None, :])).to(torch.float16)
+    assert t.stride(0) in (0, 512)
+    assert cr._ld(t) == 512
+    assert cr._ld(torch.zeros(3, 40)[:, :16]) == 40
