@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from an ncu capture of
 # this kernel; valid only while code_sha16(gemm.cu) equals this (the hash ignores comments;
 # otherwise the bench line reports traffic as null).
-GEMM_TRAFFIC = {"sha256_16": "67114e11caa6a2e2", "bytes": 3029191168 + 905975296}
+GEMM_TRAFFIC = {"sha256_16": "b3110dca79e8ac91", "bytes": 2818213120 + 848316160}
 
 
 def code_sha16(path: str) -> str:
@@ -590,18 +590,23 @@ def time_controls(wl: synth.Workload, dev, world, flush, warmup, steps=20):
     return out
 
 
-def time_library_controls(wl: synth.Workload, dev, flush, warmup, steps=20):
-    """Library controls, timed the way the layer's GEMM is (L2 flushed before
-    every call, CUDA events on the launching stream), off the product path:
-    - cublas_fp16: torch.matmul in FP16 on the GEMM's own shape (M x K_p) x
-      (K_p x N), the same tensor-core route and operand width as the layer's
-      GEMM;
-    - int8_mm: torch._int_mm (cuBLASLt S8 x S8 -> int32) on the same shape and
-      at 8192^3: the rate of the S8 tensor path this GPU offers through the
-      library, the denominator of an "INT8 roofline"."""
+def time_library_controls(layer: "Layer", flush, warmup, steps=20):
+    """Library controls on the layer's own operands, timed the way the layer's
+    GEMM is (L2 flushed before every call, CUDA events on the launching
+    stream), off the product path:
+    - cublas_fp16: torch.matmul of the layer's FP16-held activation and weight
+      codes, (M x K_p) x (K_p x N): the same tensor-core route, operand width
+      and values (the codes' magnitudes set the tensor cores' power draw) as
+      the layer's GEMM;
+    - int8_mm: torch._int_mm (cuBLASLt S8 x S8 -> int32) on the same codes as
+      int8, and on random codes at 8192^3: the rate of the S8 tensor path
+      this GPU offers through the library, the denominator of an "INT8
+      roofline"."""
     import torch
-    M, N, Kp = wl.M, wl.N, -(-wl.K // 256) * 256
-    g = torch.Generator(device=dev).manual_seed(7)
+    A, B = layer.aq, layer.wq
+    M, Kp = A.shape
+    N = B.shape[0]
+    dev = A.device
 
     def timed(fn, n):
         for _ in range(warmup):
@@ -621,16 +626,18 @@ def time_library_controls(wl: synth.Workload, dev, flush, warmup, steps=20):
         return tot / n
 
     out = {}
-    A = torch.randint(-127, 128, (M, Kp), generator=g, device=dev).to(torch.float16)
-    B = torch.randint(-127, 128, (N, Kp), generator=g, device=dev).to(torch.float16)
     ms = timed(lambda: torch.matmul(A, B.t()), steps)
-    out["cublas_fp16"] = {"shape": f"{M}x{N}x{Kp}", "ms": ms, "tflops": 2.0 * M * N * Kp / (ms / 1e3) / 1e12}
-    del A, B
+    out["cublas_fp16"] = {"shape": f"{M}x{N}x{Kp}", "operands": "the layer's FP16-held codes", "ms": ms,
+                          "tflops": 2.0 * M * N * Kp / (ms / 1e3) / 1e12}
     torch.cuda.empty_cache()
+    g = torch.Generator(device=dev).manual_seed(7)
     for name, (m, n, k) in (("int8_mm", (M, N, Kp)), ("int8_mm_8192", (8192, 8192, 8192))):
         try:
-            A8 = torch.randint(-127, 128, (m, k), generator=g, device=dev, dtype=torch.int8)
-            B8 = torch.randint(-127, 128, (n, k), generator=g, device=dev, dtype=torch.int8)
+            if name == "int8_mm":
+                A8, B8 = A.to(torch.int8), B.to(torch.int8)
+            else:
+                A8 = torch.randint(-127, 128, (m, k), generator=g, device=dev, dtype=torch.int8)
+                B8 = torch.randint(-127, 128, (n, k), generator=g, device=dev, dtype=torch.int8)
             ms = timed(lambda: torch._int_mm(A8, B8.t()), 5)
             out[name] = {"shape": f"{m}x{n}x{k}", "ms": ms, "tops": 2.0 * m * n * k / (ms / 1e3) / 1e12}
             del A8, B8
@@ -857,10 +864,9 @@ def main():
         sustained["gemm_frac_of_sustained_peak"] = sustained["gemm_tflops"] / peak_sust
     if layer.cr.device_error() != 0:
         raise SystemExit("device timeout reported by the GEMM")
+    library = time_library_controls(layer, flush, args.warmup) if args.library else None
     del layer
     torch.cuda.empty_cache()
-
-    library = time_library_controls(wl, dev, flush, args.warmup) if args.library else None
 
     secondary = None
     if args.secondary:
