@@ -71,6 +71,17 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------- workload sizes
+def norms_pay(Kp: int) -> bool:
+    """Whether the layer asks the quantisation kernels for code-norm bounds.
+    They cost the kernels a sum of squares (2-5% of their time) and let the
+    GEMM run a tile as one FP32 chunk when max bound(A) x max bound(B) < 2^24.
+    Rotated rows of ordinary data have codes with an RMS of about 30-36, so a
+    bound near 33 sqrt(K_p): the product stays below 2^24 up to K_p of about
+    8192-13000 (QKV, K_p = 5376: about 2300 each) and not at K_p = 14336
+    (FFN-down: about 4200 each), where the bounds would cost without paying."""
+    return Kp <= 8192
+
+
 def layer_sizes(wl: synth.Workload):
     """Work of one layer.  act_alg / w_alg are the algorithmic bytes of the
     two quantisation kernels with one-byte S8 codes (inputs read once, codes
@@ -81,9 +92,11 @@ def layer_sizes(wl: synth.Workload):
     esz = {"bf16": 2, "fp16": 2, "fp32": 4}
     act_in = wl.M * wl.k_in * esz[wl.x_dtype]
     w_in = wl.N * Ks // 2 + wl.N * Ks // 16
+    nb = 4 if norms_pay(Kp) else 0          # the norm bounds, when requested
     return dict(Kp=Kp, Ks=Ks, ops=2.0 * wl.M * wl.N * wl.K, gemm_flops=2.0 * wl.M * wl.N * Kp,
                 act_alg=act_in + wl.M * Kp + 4 * wl.M, w_alg=w_in + wl.N * Kp + 4 * wl.N,
-                act_bytes=act_in + wl.M * Kp * 2 + 4 * wl.M, w_bytes=w_in + 4 + wl.N * Kp * 2 + 4 * wl.N)
+                act_bytes=act_in + wl.M * Kp * 2 + (4 + nb) * wl.M,
+                w_bytes=w_in + 4 + wl.N * Kp * 2 + (4 + nb) * wl.N)
 
 
 # ---------------------------------------------------------------- clocks
@@ -208,20 +221,24 @@ class Layer:
         Kp = self.sz["Kp"]
         self.aq = torch.empty(wl.M, Kp, dtype=torch.float16, device=dev)
         self.sa = torch.empty(wl.M, dtype=torch.float32, device=dev)
+        # code-norm bounds, requested only where they can pay (norms_pay)
+        use = norms_pay(Kp)
+        self.na = torch.empty(wl.M, dtype=torch.float32, device=dev) if use else None
         self.wq = torch.empty(wl.N, Kp, dtype=torch.float16, device=dev)
         self.sw = torch.empty(wl.N, dtype=torch.float32, device=dev)
+        self.nw = torch.empty(wl.N, dtype=torch.float32, device=dev) if use else None
         self.y = torch.empty(wl.M, wl.N, dtype=tdt[wl.out_dtype], device=dev)
         self.h_y = None
         self.in_bytes = sum(t.numel() * t.element_size() for t in (self.h_x, self.h_p, self.h_s, self.h_t))
 
     def weight(self):
-        self.cr.prepare_weight(self.p, self.s, self.t, self.wl.K, self.wq, self.sw)
+        self.cr.prepare_weight(self.p, self.s, self.t, self.wl.K, self.wq, self.sw, w_norm=self.nw)
 
     def act(self):
-        self.cr.quant_act(self.x, self.wl.K, self.aq, self.sa, swiglu=self.wl.swiglu)
+        self.cr.quant_act(self.x, self.wl.K, self.aq, self.sa, swiglu=self.wl.swiglu, a_norm=self.na)
 
     def gemm(self):
-        self.cr.gemm(self.aq, self.sa, self.wq, self.sw, self.y)
+        self.cr.gemm(self.aq, self.sa, self.wq, self.sw, self.y, a_norm=self.na, w_norm=self.nw)
 
     def step(self):
         self.weight()
@@ -363,9 +380,9 @@ class E2EPipeline:
                 self.s_run.wait_event(in_done[k])
                 if out_done[k] is not None:
                     self.s_run.wait_event(out_done[k])
-                L.cr.prepare_weight(b["p"], b["s"], b["t"], L.wl.K, L.wq, L.sw)
-                L.cr.quant_act(b["x"], L.wl.K, L.aq, L.sa, swiglu=L.wl.swiglu)
-                L.cr.gemm(L.aq, L.sa, L.wq, L.sw, b["y"])
+                L.cr.prepare_weight(b["p"], b["s"], b["t"], L.wl.K, L.wq, L.sw, w_norm=L.nw)
+                L.cr.quant_act(b["x"], L.wl.K, L.aq, L.sa, swiglu=L.wl.swiglu, a_norm=L.na)
+                L.cr.gemm(L.aq, L.sa, L.wq, L.sw, b["y"], a_norm=L.na, w_norm=L.nw)
                 run_done[k] = ev()
                 run_done[k].record(self.s_run)
             parts = self.s_out_parts
@@ -493,22 +510,26 @@ def time_ffn_block(dev, world, flush, warmup, steps=10):
     Hp, Fp = cr.padded_k(H), cr.padded_k(F)
     w1 = torch.empty(2 * F, Hp, dtype=torch.float16, device=dev)
     sw1 = torch.empty(2 * F, dtype=torch.float32, device=dev)
+    nw1 = torch.empty(2 * F, dtype=torch.float32, device=dev) if norms_pay(Hp) else None
     w2 = torch.empty(H, Fp, dtype=torch.float16, device=dev)
     sw2 = torch.empty(H, dtype=torch.float32, device=dev)
+    nw2 = torch.empty(H, dtype=torch.float32, device=dev) if norms_pay(Fp) else None
     xq = torch.empty(M, Hp, dtype=torch.float16, device=dev)
     sx = torch.empty(M, dtype=torch.float32, device=dev)
+    nx = torch.empty(M, dtype=torch.float32, device=dev) if norms_pay(Hp) else None
     h2 = torch.empty(M, 2 * F, dtype=torch.bfloat16, device=dev)
     hq = torch.empty(M, Fp, dtype=torch.float16, device=dev)
     sh = torch.empty(M, dtype=torch.float32, device=dev)
+    nh = torch.empty(M, dtype=torch.float32, device=dev) if norms_pay(Fp) else None
     y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
 
     def step():
-        cr.prepare_weight(P1, S1, T1, H, w1, sw1)
-        cr.quant_act(xd, H, xq, sx)
-        cr.gemm(xq, sx, w1, sw1, h2)
-        cr.prepare_weight(P2, S2, T2, F, w2, sw2)
-        cr.quant_act(h2, F, hq, sh, swiglu=True)
-        cr.gemm(hq, sh, w2, sw2, y)
+        cr.prepare_weight(P1, S1, T1, H, w1, sw1, w_norm=nw1)
+        cr.quant_act(xd, H, xq, sx, a_norm=nx)
+        cr.gemm(xq, sx, w1, sw1, h2, a_norm=nx, w_norm=nw1)
+        cr.prepare_weight(P2, S2, T2, F, w2, sw2, w_norm=nw2)
+        cr.quant_act(h2, F, hq, sh, swiglu=True, a_norm=nh)
+        cr.gemm(hq, sh, w2, sw2, y, a_norm=nh, w_norm=nw2)
 
     for _ in range(warmup):
         flush()
@@ -554,7 +575,7 @@ def time_controls(wl: synth.Workload, dev, world, flush, warmup, steps=20):
     def w8a8():
         cr.widen_codes(wq8, L.wq, cols=Kp)
         L.act()
-        L.gemm()
+        L.gemm()                    # the weight-norm bounds of L.weight() above still hold
 
     def resident():
         L.act()
@@ -562,8 +583,8 @@ def time_controls(wl: synth.Workload, dev, world, flush, warmup, steps=20):
 
     def ps_bias():
         L.weight()
-        cr.quant_act(L.x, wl.K, L.aq, L.sa, swiglu=wl.swiglu, pre_scale=pre)
-        cr.gemm(L.aq, L.sa, L.wq, L.sw, L.y, bias=bias)
+        cr.quant_act(L.x, wl.K, L.aq, L.sa, swiglu=wl.swiglu, pre_scale=pre, a_norm=L.na)
+        cr.gemm(L.aq, L.sa, L.wq, L.sw, L.y, bias=bias, a_norm=L.na, w_norm=L.nw)
 
     out = {}
     for name, fn in (("w8a8_resident_s8", w8a8), ("resident_f16_codes", resident), ("prescale_bias", ps_bias)):
@@ -753,8 +774,8 @@ def bench_config(wl: synth.Workload, overlap: int) -> dict:
                       if overlap else "NVFP4 weight prep + act rotation/S8 + GEMM per step"),
             "l2": "flushed before every step (a write of twice the L2 size)",
             "parallelism": "single GPU",
-            "arith": "S8 codes held as FP16 on tcgen05 kind::f16, exact int32 via 1024-K FP32 chunks; "
-                     "FP32 rotation"}
+            "arith": "S8 codes held as FP16 on tcgen05 kind::f16, exact int32 (one FP32 chunk per tile where "
+                     "the rows' code-norm bounds allow it, else chunks of at most 1024); FP32 rotation"}
 
 
 # ---------------------------------------------------------------- main
@@ -850,6 +871,16 @@ def main():
         "quant_act": quant_kernel(1e3 * a_ms, sz["act_alg"], sz["act_bytes"]),
         "gemm": {"ms": g_ms, "tflops": achieved},
     }
+    # Decode inside the GEMM: a GEMM whose producers decode, rotate and quantise
+    # the NVFP4 weight itself has to redo that work for every 256-row strip of
+    # tokens that meets a weight tile (no strip can keep a 256 x K_p tile of
+    # codes resident).  At the whole-GPU rate the weight kernel measured just
+    # now, that work alone takes strips x its time, with perfect overlap and no
+    # interference with the MMAs assumed, plus a scales-only pre-pass.
+    strips = -(-wl.M // 256)
+    decode_in_gemm = {"m_strips": strips, "redone_weight_work_ms": strips * w_ms,
+                      "vs_layer_ms": ms_step,
+                      "note": "lower bound on a decode-inside-GEMM layer from this run's weight-kernel time"}
 
     # end-to-end through the public API with host buffers
     e2e_value = e2e_ms = link = None
@@ -943,6 +974,7 @@ def main():
         "ms_per_layer": ms_step,
         "ms_per_layer_serial": serial_ms,
         "kernels": kernels,
+        "decode_inside_gemm_bound": decode_in_gemm,
         "roofline": roofline,
         "hbm_peak_gbs": hbm,
         "hbm_note": ("quant kernels: hbm_frac on algorithmic bytes with 1-byte S8 codes; moved_* on the bytes "

@@ -95,6 +95,9 @@ const char* convrot_status_string(int status);
  *   w_q     [N][ld_wq] codes in `fmt`, columns 0..K_p-1 written (the zero
  *           padding included); ld_wq >= K_p.
  *   w_scale [N] FP32 row scales s_w (0 for a degenerate row).
+ *   w_norm  NULL, or [N] FP32 (4-byte aligned): an upper bound on the
+ *           Euclidean norm of each row's codes, for convrot_gemm (see there;
+ *           the cost and the codes as for convrot_quant_act's a_norm).
  *
  * Decoded weight w = E2M1 * E4M3 * t.  Per row: r = rotate(w padded to K_p);
  * s_w = fp32(max|r| / 127); q = clamp(rint(r * fp32(1/s_w)), -127, 127), the
@@ -107,7 +110,7 @@ const char* convrot_status_string(int status);
 int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
                            const float* w_tensor_scale, int N, int K,
                            void* w_q, convrot_codes fmt, int64_t ld_wq,
-                           float* w_scale, cudaStream_t stream);
+                           float* w_scale, float* w_norm, cudaStream_t stream);
 
 /*
  * Activation quantisation: optional SwiGLU prologue, optional channel
@@ -129,6 +132,12 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
  *           the rotation, in FP32).
  *   a_q     [M][ld_aq] codes in `fmt`, columns 0..K_p-1 written; ld_aq >= K_p.
  *   a_scale [M] FP32 token scales s_a (0 for a degenerate row).
+ *   a_norm  NULL, or [M] FP32 (4-byte aligned): an upper bound on the
+ *           Euclidean norm of each row's codes, for convrot_gemm.  Asking
+ *           for it adds a sum of squares to the kernel (a few percent of its
+ *           time); it pays where the bounds let the GEMM skip its chunk
+ *           drains, i.e. for ordinary rotated data up to K_p of about 8192.
+ *           The codes and scales are the same either way.
  *
  * Quantiser as for the weights (FP32 scale, FP32 reciprocal, FP32 product,
  * round half to even, clamp to +-127).  A row holding an Inf or NaN value
@@ -140,7 +149,7 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
 int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
                       int M, int K, int swiglu, const float* pre_scale,
                       void* a_q, convrot_codes fmt, int64_t ld_aq,
-                      float* a_scale, cudaStream_t stream);
+                      float* a_scale, float* a_norm, cudaStream_t stream);
 
 /*
  * Integer GEMM with the dequantising epilogue.  Source: the NVFP4 loader
@@ -152,6 +161,18 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
  *   a_q     [M][ld_aq] FP16-stored S8 codes of the rotated activations.
  *   w_q     [N][ld_wq] FP16-stored S8 codes of the rotated weights.
  *   a_scale [M], w_scale [N] FP32 row scales (w_scale 16-byte aligned).
+ *   a_norm, w_norm  NULL, or the [M] and [N] code-norm bounds written by
+ *           convrot_quant_act and convrot_prepare_weight (4-byte aligned).
+ *           The tensor cores accumulate in FP32, so the int32 result is exact
+ *           only while every partial sum stays below 2^24.  Without the
+ *           bounds the K loop is cut into exact chunks of at most 1024
+ *           (127^2 * 1024 < 2^24), each drained to int32.  With them, a
+ *           256 x 256 output tile whose largest a_norm times largest w_norm
+ *           is below 2^24 runs as one chunk: by Cauchy-Schwarz every partial
+ *           sum of q_a[m, :] . q_w[n, :], in any order, is at most
+ *           ||q_a[m, :]|| ||q_w[n, :]||.  The result is the same int32 sum;
+ *           only the number of drains changes.  Bounds smaller than the true
+ *           norms void that guarantee.
  *   bias    NULL, or [N] FP32 per-output-channel bias (16-byte aligned).
  *   K_p     padded reduction width, a multiple of 256, <= CONVROT_MAX_KP.
  *   out     [M][ld_out] in out_dtype; ld_out >= N.  Only columns 0..N-1 of
@@ -165,7 +186,8 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
  * per-element stores).
  */
 int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale,
-                 const void* w_q, int64_t ld_wq, const float* w_scale,
+                 const float* a_norm, const void* w_q, int64_t ld_wq,
+                 const float* w_scale, const float* w_norm,
                  const float* bias, int M, int N, int K_p,
                  void* out, convrot_dtype out_dtype, int64_t ld_out,
                  cudaStream_t stream);
@@ -187,10 +209,11 @@ int convrot_widen_codes(const int8_t* src, int64_t ld_src, int rows, int cols,
 /*
  * Test hook: the same GEMM, writing the raw int32 accumulators
  * acc[m, n] = sum_k q_a[m, k] * q_w[n, k] into acc [M][ld_acc] instead of
- * dequantising.  Arguments and rules as convrot_gemm.
+ * dequantising.  Arguments and rules as convrot_gemm (a_norm and w_norm
+ * choose the chunking the same way).
  */
-int convrot_gemm_i32(const void* a_q, int64_t ld_aq,
-                     const void* w_q, int64_t ld_wq,
+int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const float* a_norm,
+                     const void* w_q, int64_t ld_wq, const float* w_norm,
                      int M, int N, int K_p,
                      int32_t* acc, int64_t ld_acc, cudaStream_t stream);
 

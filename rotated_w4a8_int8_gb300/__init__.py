@@ -49,13 +49,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.convrot_padded_k.restype = i32
     lib.convrot_status_string.argtypes = [i32]
     lib.convrot_status_string.restype = ctypes.c_char_p
-    lib.convrot_prepare_weight.argtypes = [vp, vp, vp, i32, i32, vp, i32, i64, vp, vp]
+    lib.convrot_prepare_weight.argtypes = [vp, vp, vp, i32, i32, vp, i32, i64, vp, vp, vp]
     lib.convrot_prepare_weight.restype = i32
-    lib.convrot_quant_act.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, i32, i64, vp, vp]
+    lib.convrot_quant_act.argtypes = [vp, i32, i64, i32, i32, i32, vp, vp, i32, i64, vp, vp, vp]
     lib.convrot_quant_act.restype = i32
-    lib.convrot_gemm.argtypes = [vp, i64, vp, vp, i64, vp, vp, i32, i32, i32, vp, i32, i64, vp]
+    lib.convrot_gemm.argtypes = [vp, i64, vp, vp, vp, i64, vp, vp, vp, i32, i32, i32, vp, i32, i64, vp]
     lib.convrot_gemm.restype = i32
-    lib.convrot_gemm_i32.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp, i64, vp]
+    lib.convrot_gemm_i32.argtypes = [vp, i64, vp, vp, i64, vp, i32, i32, i32, vp, i64, vp]
     lib.convrot_gemm_i32.restype = i32
     lib.convrot_widen_codes.argtypes = [vp, i64, i32, i32, vp, i64, vp]
     lib.convrot_widen_codes.restype = i32
@@ -118,40 +118,44 @@ def _codes_fmt(t) -> int:
     return {torch.int8: CODES_S8, torch.float16: CODES_F16}[t.dtype]
 
 
-def prepare_weight(w_fp4, w_sf, w_tensor_scale, K: int, w_q, w_scale, stream=None) -> None:
+def prepare_weight(w_fp4, w_sf, w_tensor_scale, K: int, w_q, w_scale, w_norm=None, stream=None) -> None:
     """convrot_prepare_weight: w_fp4 uint8 [N, K_s/2], w_sf uint8 [N, K_s/16],
-    w_tensor_scale float32 [1], w_q int8 or float16 [N, >=K_p], w_scale float32 [N]."""
+    w_tensor_scale float32 [1], w_q int8 or float16 [N, >=K_p], w_scale float32 [N],
+    w_norm None or float32 [N] (bounds on the rows' code norms, for gemm)."""
     N = w_fp4.shape[0]
     _check("convrot_prepare_weight", load_library().convrot_prepare_weight(
         _ptr(w_fp4), _ptr(w_sf), _ptr(w_tensor_scale), N, int(K), _ptr(w_q), _codes_fmt(w_q),
-        _ld(w_q), _ptr(w_scale), _stream(stream)))
+        _ld(w_q), _ptr(w_scale), _ptr(w_norm), _stream(stream)))
 
 
-def quant_act(x, K: int, a_q, a_scale, swiglu: bool = False, pre_scale=None, stream=None) -> None:
+def quant_act(x, K: int, a_q, a_scale, swiglu: bool = False, pre_scale=None, a_norm=None, stream=None) -> None:
     """convrot_quant_act: x bf16/fp16/fp32 [M, >=K or 2K], a_q int8 or float16
-    [M, >=K_p], a_scale float32 [M], pre_scale None or float32 [K]."""
+    [M, >=K_p], a_scale float32 [M], pre_scale None or float32 [K], a_norm None
+    or float32 [M] (bounds on the rows' code norms, for gemm)."""
     M = x.shape[0]
     _check("convrot_quant_act", load_library().convrot_quant_act(
         _ptr(x), _dtype_code(x), _ld(x), M, int(K), int(bool(swiglu)), _ptr(pre_scale),
-        _ptr(a_q), _codes_fmt(a_q), _ld(a_q), _ptr(a_scale), _stream(stream)))
+        _ptr(a_q), _codes_fmt(a_q), _ld(a_q), _ptr(a_scale), _ptr(a_norm), _stream(stream)))
 
 
-def gemm(a_q, a_scale, w_q, w_scale, out, K_p: int | None = None, bias=None, stream=None) -> None:
+def gemm(a_q, a_scale, w_q, w_scale, out, K_p: int | None = None, bias=None, a_norm=None, w_norm=None,
+         stream=None) -> None:
     """convrot_gemm: a_q float16 codes [M, >=K_p], w_q float16 codes [N, >=K_p],
-    out bf16/fp16/fp32 [M, >=N] (N = w_q rows), bias None or float32 [N]."""
+    out bf16/fp16/fp32 [M, >=N] (N = w_q rows), bias None or float32 [N],
+    a_norm / w_norm None or the code-norm bounds from quant_act / prepare_weight."""
     M, N = a_q.shape[0], w_q.shape[0]
     K_p = a_q.shape[1] if K_p is None else K_p
     _check("convrot_gemm", load_library().convrot_gemm(
-        _ptr(a_q), _ld(a_q), _ptr(a_scale), _ptr(w_q), _ld(w_q), _ptr(w_scale),
+        _ptr(a_q), _ld(a_q), _ptr(a_scale), _ptr(a_norm), _ptr(w_q), _ld(w_q), _ptr(w_scale), _ptr(w_norm),
         _ptr(bias), M, N, int(K_p), _ptr(out), _dtype_code(out), _ld(out), _stream(stream)))
 
 
-def gemm_i32(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:
+def gemm_i32(a_q, w_q, acc, K_p: int | None = None, a_norm=None, w_norm=None, stream=None) -> None:
     """convrot_gemm_i32: raw int32 accumulators into acc int32 [M, >=N]."""
     M, N = a_q.shape[0], w_q.shape[0]
     K_p = a_q.shape[1] if K_p is None else K_p
     _check("convrot_gemm_i32", load_library().convrot_gemm_i32(
-        _ptr(a_q), _ld(a_q), _ptr(w_q), _ld(w_q), M, N, int(K_p), _ptr(acc),
+        _ptr(a_q), _ld(a_q), _ptr(a_norm), _ptr(w_q), _ld(w_q), _ptr(w_norm), M, N, int(K_p), _ptr(acc),
         _ld(acc), _stream(stream)))
 
 

@@ -16,7 +16,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libconvrot.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu"]
+# (source, object, defines): quant.cu is compiled twice, once without and once
+# with the kernels that write code-norm bounds
+SOURCES = [("api.cu", "api", []), ("quant.cu", "quant", []),
+           ("quant.cu", "quant_norm", ["-DCONVROT_QUANT_NORM=1"]), ("gemm.cu", "gemm", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]
@@ -29,9 +32,10 @@ def nvcc() -> str:
     return cand
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(unit, extra: list[str]) -> str:
+    src, name, defines = unit
+    obj = os.path.join(BUILD, name + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, *defines, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")

@@ -19,7 +19,9 @@
 // that are odd and above 2^23).  The K loop is therefore cut into 1024-wide
 // chunks, each accumulated afresh in one of two TMEM buffers; epilogue warps
 // convert each finished chunk to int32 (exact) and add it to per-thread int32
-// registers while the tensor core fills the other buffer.
+// registers while the tensor core fills the other buffer.  Given bounds on
+// the rows' code norms, a work item whose bounds keep every partial sum
+// below 2^24 (Cauchy-Schwarz) runs its whole K loop as one chunk.
 //
 // Mainloop: the MMA runs on CTA pairs (tcgen05.mma.cta_group::2, M = 256,
 // N = 256, K = 16).  Each CTA of a pair holds its own 128 rows of A and one
@@ -39,7 +41,9 @@
 // Warp 0: TMA producer.  Warp 1: TMEM owner and (even CTA) MMA issuer.
 // Warps 2..9: epilogue, which applies y = fp32(acc) * s_a * s_w (+ bias),
 // stages 32-row x 64-byte boxes in swizzled shared memory and writes them
-// with TMA tensor stores (per-element stores for unaligned outputs).  Every
+// with TMA tensor stores (per-element stores for unaligned outputs).
+// Warp 10 (even CTA, with norm bounds): evaluates the chunk count of the
+// coming work items ahead of the MMA issuer.  Every
 // mbarrier wait is bounded: after about two seconds the waiting role records
 // an error code, the CTA drains what it has in flight and returns.
 #include <cstdint>
@@ -63,7 +67,13 @@ constexpr int B_BYTES = (BN / 2) * BK * 2;       // 16 KiB: this CTA's half (128
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KiB per CTA
 constexpr int PAIR_STAGE_BYTES = 2 * STAGE_BYTES;// bytes landing in both CTAs of a pair per stage
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int THREADS = 64 + NUM_EPI_WARPS * 32; // 320
+constexpr int NORM_WARP = 2 + NUM_EPI_WARPS;     // warp 10: chunking of the coming work items
+constexpr int THREADS = 64 + NUM_EPI_WARPS * 32 + 32;   // 352
+// Eleven warps put at most three on one SM sub-partition (16K registers):
+// the launch bound is declared for 384 threads so that the compiler keeps a
+// thread at 168 registers (3 x 32 x 168 <= 16384).
+constexpr int THREADS_BOUND = 384;
+constexpr int NRING = 4;                         // chunk counts evaluated ahead of the MMA issuer
 constexpr int TMEM_COLS = 512;                   // two 256-column FP32 buffers
 constexpr int NPAIRS = 1;                        // CTA pairs per cluster (2: they share A by multicast)
 constexpr int CLUSTER = 2 * NPAIRS;              // rank = 2 * pair + half
@@ -78,10 +88,11 @@ constexpr int OUT_BUFS = 2;
 constexpr int OUT_STAGING = NUM_EPI_WARPS * OUT_BUFS * OUT_BOX;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + OUT_STAGING + 1024 /*align*/ + 256 /*barriers*/;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+static_assert((2 * STAGES + 7 + 2 * NRING) * 8 + NRING * 4 <= 256, "barrier area");
 
 // Codes recorded in g_error: which wait ran out first.
 enum ErrCode : int { ERR_NONE = 0, ERR_WAIT_FULL = 1, ERR_WAIT_EMPTY = 2, ERR_WAIT_ACC_FULL = 3,
-                     ERR_WAIT_ACC_EMPTY = 4 };
+                     ERR_WAIT_ACC_EMPTY = 4, ERR_WAIT_CHUNKS = 5 };
 
 __device__ int g_error = 0;   // first failure code of any GEMM launch (0 = none)
 
@@ -173,6 +184,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
 // hand a drained TMEM buffer back to the pair's MMA issuer, and the tensor
 // memory reads it orders are fenced by tcgen05.fence::before_thread_sync (a
 // cluster-scope release here made every arrive a cluster-wide memory fence).
+// Arrive on a barrier of this CTA (release at CTA scope: writes before it are
+// seen by a thread whose wait completes the phase).
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
@@ -280,6 +297,8 @@ struct Params {
   const float* a_scale;
   const float* w_scale;
   const float* bias;   // optional, [N]
+  const float* a_norm; // optional, [M]: bounds on the Euclidean norms of A's rows of codes
+  const float* w_norm; // optional, [N]: the same for B's rows
   void* out;
   int64_t ld_out;
   int out_vec;      // 16-byte vector stores allowed (base and pitch aligned)
@@ -321,6 +340,40 @@ __device__ __forceinline__ bool work_coords(const Params& p, int item, int pair,
   return false;
 }
 
+// ------------------------------------------------------------------ chunking of a work item
+// Every partial sum of a dot product q_a[m, :] . q_w[n, :], in any order, is
+// at most ||q_a[m, :]|| ||q_w[n, :]|| (Cauchy-Schwarz).  When the largest
+// bound among the work item's 256 A rows times the largest among its 256 B
+// rows is below 2^24, every FP32 partial sum of the tile is an exact integer,
+// so the whole K loop runs as one chunk; otherwise it is cut into exact
+// chunks of at most KCHUNK_STEPS.  A warp evaluates it (lane l reads rows
+// l, l + 32, ...): the chunking warp for the MMA issuer, each epilogue warp
+// for itself; all reach the same answer for an item.
+__device__ __forceinline__ int tile_chunks(const Params& p, int m2, int nt, int lane, int default_chunks) {
+  // maxima over the bit patterns: non-negative floats (and NaN, which then
+  // fails the test) order like their bits; four rows of each operand in flight
+  uint32_t ma = 0u, mw = 0u;
+#pragma unroll 2
+  for (int j = 0; j < 8; j += 4) {
+    float a[4], w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int ra = m2 * (2 * BM) + lane + 32 * (j + u), rw = nt * BN + lane + 32 * (j + u);
+      a[u] = ra < p.M ? __ldg(p.a_norm + ra) : 0.f;
+      w[u] = rw < p.N ? __ldg(p.w_norm + rw) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      ma = max(ma, __float_as_uint(a[u]) & 0x7fffffffu);
+      mw = max(mw, __float_as_uint(w[u]) & 0x7fffffffu);
+    }
+  }
+  ma = __reduce_max_sync(0xffffffffu, ma);
+  mw = __reduce_max_sync(0xffffffffu, mw);
+  const float prod = __fmul_ru(__uint_as_float(ma), __uint_as_float(mw));   // rounded up
+  return prod < 16777216.0f ? 1 : default_chunks;
+}
+
 // ------------------------------------------------------------------ epilogue stores
 template <int OUT>
 struct OutT;
@@ -352,19 +405,23 @@ template <> __device__ __forceinline__ uint32_t to_out2<CONVROT_FP16>(float y0, 
 // TMA_OUT: staged output boxes go out by TMA tensor stores (output base and
 // pitch 16-byte aligned); otherwise the warp writes them with element stores.
 template <int OUT, bool BIAS, bool TMA_OUT>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS_BOUND, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
             const __grid_constant__ CUtensorMap tmap_out, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + STAGES * STAGE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(staging + OUT_STAGING);
-  // barrier slots: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  // barrier slots: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain, then the
+  // TMEM address, the abort flag, the chunk-count ring's full[NRING] and empty[NRING] and
+  // the ring itself
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
   const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
   const uint32_t drain = smem_u32(bars + 2 * STAGES + 4);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 6);
+  const uint32_t nfull0 = smem_u32(bars + 2 * STAGES + 7), nempty0 = smem_u32(bars + 2 * STAGES + 7 + NRING);
+  volatile int* ring = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 7 + 2 * NRING);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -382,6 +439,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       mbar_init(acce0 + 8 * b, 2 * NUM_EPI_WARPS);   // epilogue warps of both CTAs of the pair
     }
     mbar_init(drain, 1);
+    for (int r = 0; r < NRING; ++r) {
+      mbar_init(nfull0 + 8 * r, 1);              // the chunking warp wrote ring[r]
+      mbar_init(nempty0 + 8 * r, 1);             // the MMA issuer has read it
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -409,11 +470,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
   const uint16_t a_mask = static_cast<uint16_t>(NPAIRS == 2 ? (1u << half) | (1u << (half + 2)) : 0u);
 
   const int k_steps = p.k_steps;
-  // K steps are split into equal chunks of at most KCHUNK_STEPS: a short last
+  // Without norm bounds (or when they do not allow a single chunk) the K
+  // steps are split into equal chunks of at most KCHUNK_STEPS: a short last
   // chunk would leave the epilogue less time to drain the buffer it follows
-  // (K = 5376: six chunks of 896 instead of five of 1024 and one of 256)
+  // (K = 5376: six chunks of 896 instead of five of 1024 and one of 256).
   const int chunks_per_tile = (k_steps + KCHUNK_STEPS - 1) / KCHUNK_STEPS;
-  const int chunk_steps = (k_steps + chunks_per_tile - 1) / chunks_per_tile;
+  const bool eval_chunks = p.a_norm != nullptr && p.w_norm != nullptr && chunks_per_tile > 1;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (both CTAs)
@@ -468,19 +530,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (even CTA)
-    if (lane == 0 && is_leader) {
+    // Lane 0 issues.  With norm bounds, each work item's chunk count comes
+    // from the chunking warp through the ring; evaluating it here put about
+    // 0.8 us between two items' MMAs (3% at K = 5376).
+    if (is_leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t chunk = 0;          // running chunk counter -> TMEM buffer and its phase
       bool ok = true;
       bool any = false;
-      for (int tile = cluster_id; tile < p.num_items && ok; tile += num_clusters) {
-        for (int c = 0; c < chunks_per_tile && ok; ++c, ++chunk) {
+      int item = 0;                // this cluster's work items so far -> ring slot and its phase
+      for (int tile = cluster_id; tile < p.num_items && ok; tile += num_clusters, ++item) {
+        int nchunks = chunks_per_tile;
+        if (eval_chunks) {
+          const int r = item % NRING;
+          const uint32_t use = static_cast<uint32_t>(item / NRING);
+          if (!mbar_wait(nfull0 + 8 * r, use & 1u, ERR_WAIT_CHUNKS, abort_flag)) { ok = false; break; }
+          nchunks = ring[r];
+          mbar_arrive_local(nempty0 + 8 * r);
+        }
+        const int csteps = (k_steps + nchunks - 1) / nchunks;
+        for (int c = 0; c < nchunks && ok; ++c, ++chunk) {
           const uint32_t buf = chunk & 1u, use = chunk >> 1;
           if (!mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, ERR_WAIT_ACC_EMPTY, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
-          const int ks0 = c * chunk_steps, ks1 = min(k_steps, ks0 + chunk_steps);
+          const int ks0 = c * csteps, ks1 = min(k_steps, ks0 + csteps);
           for (int ks = ks0; ks < ks1; ++ks) {
             if (!mbar_wait(full0 + 8 * stage, phase, ERR_WAIT_FULL, abort_flag)) { ok = false; break; }
             tc_fence_after();
@@ -505,6 +580,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         while (!mbar_try_wait(drain, 0) && globaltimer() - t0 < kWaitLimitNs) {}
       }
     }
+  } else if (warp == NORM_WARP) {
+    // ---------------------------------------------------------------- chunking (even CTA)
+    // Evaluates the chunk count of this cluster's work items up to NRING
+    // ahead of the MMA issuer and hands them over through ring[].
+    if (is_leader && eval_chunks) {
+      int item = 0;
+      for (int tile = cluster_id; tile < p.num_items; tile += num_clusters, ++item) {
+        const int r = item % NRING;
+        const uint32_t use = static_cast<uint32_t>(item / NRING);
+        int got = 1;
+        if (lane == 0) got = mbar_wait(nempty0 + 8 * r, (use & 1u) ^ 1u, ERR_WAIT_CHUNKS, abort_flag) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, got, 0)) break;
+        int m2, nt;
+        work_coords(p, tile, static_cast<int>(pair), m2, nt);
+        const int n = tile_chunks(p, m2, nt, lane, chunks_per_tile);
+        if (lane == 0) {
+          ring[r] = n;
+          mbar_arrive_local(nfull0 + 8 * r);
+        }
+      }
+    }
   } else {
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - 2;                  // 0..7
@@ -519,10 +615,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
       int m2, nt;
       work_coords(p, tile, static_cast<int>(pair), m2, nt);
       const int mb = 2 * m2 + static_cast<int>(half), nb = nt;
+      int nchunks = chunks_per_tile;
+      if (eval_chunks) {
+        // the chunking warp's evaluation, repeated: its loads wait in the
+        // shadow of this item's first accumulator (measured free)
+        nchunks = tile_chunks(p, m2, nt, lane, chunks_per_tile);
+      }
       int32_t acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0;
-      for (int c = 0; c < chunks_per_tile; ++c, ++chunk) {
+      for (int c = 0; c < nchunks; ++c, ++chunk) {
         const uint32_t buf = chunk & 1u, use = chunk >> 1;
         // one lane polls, the warp follows: tcgen05.ld below needs a converged warp
         int got = 1;
@@ -782,12 +884,15 @@ static int validate_operands(const void* a_q, int64_t ld_aq, const void* w_q, in
   return CONVROT_OK;
 }
 
-static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scale, const void* w_q,
-               int64_t ld_wq, const float* w_scale, const float* bias, int M, int N, int K_p, void* out,
-               int64_t ld_out, size_t out_esize, cudaStream_t stream, int test_stall = 0) {
+static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scale, const float* a_norm,
+               const void* w_q, int64_t ld_wq, const float* w_scale, const float* w_norm, const float* bias,
+               int M, int N, int K_p, void* out, int64_t ld_out, size_t out_esize, cudaStream_t stream,
+               int test_stall = 0) {
   Params p;
   p.test_stall = test_stall;
   p.bias = bias;
+  p.a_norm = a_norm;
+  p.w_norm = w_norm;
   p.M = M;
   p.N = N;
   p.K_p = K_p;
@@ -829,9 +934,17 @@ static int run(int out_kind, const void* a_q, int64_t ld_aq, const float* a_scal
 
 using namespace crgemm;
 
-extern "C" int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale, const void* w_q,
-                            int64_t ld_wq, const float* w_scale, const float* bias, int M, int N, int K_p,
-                            void* out, convrot_dtype out_dtype, int64_t ld_out, cudaStream_t stream) {
+// Norm bounds: both or neither are used; 4-byte aligned.
+static int check_norms(const float* a_norm, const float* w_norm) {
+  if (reinterpret_cast<uintptr_t>(a_norm) % 4 || reinterpret_cast<uintptr_t>(w_norm) % 4)
+    return CONVROT_ERR_MISALIGNED;
+  return CONVROT_OK;
+}
+
+extern "C" int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale, const float* a_norm,
+                            const void* w_q, int64_t ld_wq, const float* w_scale, const float* w_norm,
+                            const float* bias, int M, int N, int K_p, void* out, convrot_dtype out_dtype,
+                            int64_t ld_out, cudaStream_t stream) {
   if (out_dtype != CONVROT_BF16 && out_dtype != CONVROT_FP16 && out_dtype != CONVROT_FP32)
     return CONVROT_ERR_UNSUPPORTED;
   int st = validate_operands(a_q, ld_aq, w_q, ld_wq, M, N, K_p);
@@ -844,18 +957,23 @@ extern "C" int convrot_gemm(const void* a_q, int64_t ld_aq, const float* a_scale
   if (reinterpret_cast<uintptr_t>(out) % es || reinterpret_cast<uintptr_t>(a_scale) % 4 ||
       reinterpret_cast<uintptr_t>(w_scale) % 16 || reinterpret_cast<uintptr_t>(bias) % 16)
     return CONVROT_ERR_MISALIGNED;
-  return run(out_dtype, a_q, ld_aq, a_scale, w_q, ld_wq, w_scale, bias, M, N, K_p, out, ld_out, es, stream);
+  if ((st = check_norms(a_norm, w_norm)) != CONVROT_OK) return st;
+  return run(out_dtype, a_q, ld_aq, a_scale, a_norm, w_q, ld_wq, w_scale, w_norm, bias, M, N, K_p, out, ld_out, es,
+             stream);
 }
 
-extern "C" int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const void* w_q, int64_t ld_wq, int M,
-                                int N, int K_p, int32_t* acc, int64_t ld_acc, cudaStream_t stream) {
+extern "C" int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const float* a_norm, const void* w_q,
+                                int64_t ld_wq, const float* w_norm, int M, int N, int K_p, int32_t* acc,
+                                int64_t ld_acc, cudaStream_t stream) {
   int st = validate_operands(a_q, ld_aq, w_q, ld_wq, M, N, K_p);
   if (st != CONVROT_OK) return st;
   if (ld_acc < N) return CONVROT_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return CONVROT_OK;
   if (!acc) return CONVROT_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(acc) % 4) return CONVROT_ERR_MISALIGNED;
-  return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, nullptr, M, N, K_p, acc, ld_acc, 4, stream);
+  if ((st = check_norms(a_norm, w_norm)) != CONVROT_OK) return st;
+  return run(-1, a_q, ld_aq, nullptr, a_norm, w_q, ld_wq, nullptr, w_norm, nullptr, M, N, K_p, acc, ld_acc, 4,
+             stream);
 }
 
 extern "C" int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, const void* w_q,
@@ -865,7 +983,8 @@ extern "C" int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, con
   if (st != CONVROT_OK) return st;
   if (M == 0 || N == 0 || !acc || ld_acc < N) return CONVROT_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(acc) % 4) return CONVROT_ERR_MISALIGNED;
-  return run(-1, a_q, ld_aq, nullptr, w_q, ld_wq, nullptr, nullptr, M, N, K_p, acc, ld_acc, 4, stream, 1);
+  return run(-1, a_q, ld_aq, nullptr, nullptr, w_q, ld_wq, nullptr, nullptr, nullptr, M, N, K_p, acc, ld_acc, 4,
+             stream, 1);
 }
 
 extern "C" int convrot_device_error(cudaStream_t stream, int* code) {

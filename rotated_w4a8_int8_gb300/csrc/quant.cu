@@ -19,6 +19,16 @@
 #include "errors.h"
 #include "rotate_quant.cuh"
 
+// This file is compiled twice.  With CONVROT_QUANT_NORM = 0 it holds the
+// kernels that write no code-norm bounds, the C-ABI entry points and the code
+// widening; with CONVROT_QUANT_NORM = 1 only the kernels that also write the
+// bounds and their launcher.  The bounds' sum of squares is a compile-time
+// choice because, even when skipped at run time, it costs the register-bound
+// weight kernel spills (a 30% slower kernel, measured) and the others time.
+#ifndef CONVROT_QUANT_NORM
+#define CONVROT_QUANT_NORM 0
+#endif
+
 namespace convrot {
 
 // ------------------------------------------------------------------ loaders
@@ -235,13 +245,13 @@ __device__ __forceinline__ void apply_pre_scale(const float* __restrict__ p, int
 
 // One activation row from its raw input: (SwiGLU,) (channel pre-scale,)
 // rotation, CTA absmax, scale and codes.  `red` is this row's reduction buffer.
-template <int DT, bool SWIGLU, int NBMAX, bool PRESCALE, int SPLIT>
+template <int DT, bool SWIGLU, int NBMAX, bool PRESCALE, int SPLIT, bool NORM>
 __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, int row, int K, int blk0,
                                         int nloc, int S, int slot, int lane8, char* my, float* red,
                                         float* xred, const float* pre_scale, void* q, int f16_codes,
-                                        int64_t ld_q, float* scale) {
+                                        int64_t ld_q, float* scale, float* norm) {
   BlockCols c[NBMAX];
-  float amax = 0.f;
+  float amax = 0.f, ss = 0.f;                    // ss: sum of squares, for the norm bound (NORM)
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int li = slot + S * i, blk = blk0 + li;
@@ -253,12 +263,19 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
       if constexpr (PRESCALE) apply_pre_scale(pre_scale, blk * kBlock + 32 * lane8, K, P);
     }
     rotate_block(P, c[i], my, lane8, active);
-    if (active) amax = absmax_cols(amax, c[i]);
+    if (active) {
+      amax = absmax_cols(amax, c[i]);
+      if constexpr (NORM) ss = sumsq_cols(ss, c[i]);
+    }
   }
   // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
-  const RowQuant rq = SPLIT == 1 ? cta_rowquant<!SWIGLU>(amax, red, 0.0625f)
-                                 : cluster_rowquant(amax, red, xred, 0.0625f);
-  if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
+  const float hsk = 0.5001f * sqrtf(static_cast<float>(((K + kBlock - 1) / kBlock) * kBlock));
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant<!SWIGLU>(amax, ss, NORM, red, 0.0625f, hsk)
+                                 : cluster_rowquant(amax, ss, NORM, red, xred, 0.0625f, hsk);
+  if (threadIdx.x == 0 && blk0 == 0) {
+    scale[row] = rq.s;
+    if constexpr (NORM) norm[row] = SPLIT == 1 ? red[18] : xred[4];
+  }
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
   const float mult = rq.r * 0.0625f;           // fp32(z * (r / 16)) == fp32((z / 16) * r)
 #pragma unroll
@@ -295,14 +312,14 @@ __device__ __forceinline__ void l2_prefetch(const char* p, size_t bytes) {
 
 // Kernel 2: one CTA per activation row, or (SPLIT == 2) a cluster of two
 // CTAs per row, each owning half of the row's blocks.
-template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE, int SPLIT>
-__global__ void __launch_bounds__(kMaxThreads)
-quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S, int pf_dist,
-                 const float* __restrict__ pre_scale, void* __restrict__ q, int f16_codes, int64_t ld_q,
-                 float* __restrict__ scale) {
+template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE, int SPLIT, bool NORM>
+__device__ __forceinline__ void quant_act_row(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks,
+                                              int S, int pf_dist, const float* __restrict__ pre_scale,
+                                              void* __restrict__ q, int f16_codes, int64_t ld_q,
+                                              float* __restrict__ scale, float* __restrict__ norm) {
   extern __shared__ __align__(16) char smem[];
-  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);   // per-warp maxima
-  float* xred = red + kMaxThreads / 32;                           // cluster exchange slot
+  float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);   // row reduction slots
+  float* xred = red + 16;                                         // cluster exchange slots
   const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
   constexpr size_t esize = (DT == DT_FP32) ? 4 : 2;
   const int row = blockIdx.x / SPLIT, part = blockIdx.x % SPLIT;
@@ -320,9 +337,33 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nbl
       l2_prefetch(static_cast<const char*>(x) + static_cast<size_t>(later) * ld_x * esize + b0, b1 - b0);
     }
   }
-  act_row<DT, SWIGLU, NBMAX, PRESCALE, SPLIT>(cur, row, K, blk0, nloc, S, slot, lane8, smem + slot * kSlotBytes,
-                                              red, xred, pre_scale, q, f16_codes, ld_q, scale);
+  act_row<DT, SWIGLU, NBMAX, PRESCALE, SPLIT, NORM>(cur, row, K, blk0, nloc, S, slot, lane8, smem + slot * kSlotBytes,
+                                              red, xred, pre_scale, q, f16_codes, ld_q, scale, norm);
   if constexpr (SPLIT == 2) cluster_exit_wait();
+}
+
+template <int DT, bool SWIGLU, int NBMAX, int VEC, bool PRESCALE, int SPLIT, bool NORM>
+__global__ void __launch_bounds__(kMaxThreads)
+quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S, int pf_dist,
+                 const float* __restrict__ pre_scale, void* __restrict__ q, int f16_codes, int64_t ld_q,
+                 float* __restrict__ scale, float* __restrict__ norm) {
+  quant_act_row<DT, SWIGLU, NBMAX, VEC, PRESCALE, SPLIT, NORM>(x, ld_x, M, K, nblocks, S, pf_dist, pre_scale, q,
+                                                               f16_codes, ld_q, scale, norm);
+}
+
+// The plain single-CTA form (no SwiGLU, one block per slot) held to 48
+// registers: 7 CTAs of a 21-block row then fit an SM instead of 6 (QKV
+// activations 76.5 -> 74.4 us, same box, alternating order; 42 registers,
+// 8 CTAs, measured slower; with the norm bound's sum of squares 86.7 -> 84.3
+// us).  The other forms keep the 512-thread launch bound alone: held to 48
+// registers, the SwiGLU form spills and ran 25% slower.
+template <int DT, int VEC, bool PRESCALE, bool NORM>
+__global__ void __maxnreg__(48)
+quant_act_kernel_r48(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S, int pf_dist,
+                     const float* __restrict__ pre_scale, void* __restrict__ q, int f16_codes, int64_t ld_q,
+                     float* __restrict__ scale, float* __restrict__ norm) {
+  quant_act_row<DT, false, 1, VEC, PRESCALE, 1, NORM>(x, ld_x, M, K, nblocks, S, pf_dist, pre_scale, q, f16_codes,
+                                                      ld_q, scale, norm);
 }
 
 // Raw NVFP4 input of one weight row for this thread.
@@ -374,12 +415,12 @@ __device__ __forceinline__ void load_weight_row(const uint8_t* w_fp4, const uint
 
 // One weight row from its raw input: decode, rotation, tensor scale, CTA
 // absmax, scale and codes.
-template <int NBMAX, int SPLIT>
+template <int NBMAX, int SPLIT, bool NORM>
 __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K, int blk0, int nloc, int S,
                                            int slot, int lane8, float t16, char* my, float* red, float* xred,
-                                           void* q, int f16_codes, int64_t ld_q, float* scale) {
+                                           void* q, int f16_codes, int64_t ld_q, float* scale, float* norm) {
   BlockCols c[NBMAX];
-  float amax = 0.f;
+  float amax = 0.f, ss = 0.f;                    // ss: sum of squares, for the norm bound (NORM)
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
     const int li = slot + S * i, blk = blk0 + li;
@@ -390,11 +431,16 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
     if (active) {
       scale_cols(c[i], t16);                   // rotated weight = fp32(z * t / 16)
       amax = absmax_cols(amax, c[i]);
+      if constexpr (NORM) ss = sumsq_cols(ss, c[i]);
     }
   }
-  const RowQuant rq = SPLIT == 1 ? cta_rowquant<true>(amax, red, 1.0f)
-                                 : cluster_rowquant(amax, red, xred, 1.0f);
-  if (threadIdx.x == 0 && blk0 == 0) scale[row] = rq.s;
+  const float hsk = 0.5001f * sqrtf(static_cast<float>(((K + kBlock - 1) / kBlock) * kBlock));
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant<true>(amax, ss, NORM, red, 1.0f, hsk)
+                                 : cluster_rowquant(amax, ss, NORM, red, xred, 1.0f, hsk);
+  if (threadIdx.x == 0 && blk0 == 0) {
+    scale[row] = rq.s;
+    if constexpr (NORM) norm[row] = SPLIT == 1 ? red[18] : xred[4];
+  }
   void* qrow = static_cast<char*>(q) + static_cast<size_t>(row) * ld_q * (f16_codes ? 2 : 1);
 #pragma unroll
   for (int i = 0; i < NBMAX; ++i) {
@@ -412,14 +458,15 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
 // of 512 threads per SM): 7 CTAs of a 21-block row then fit an SM instead of
 // 6, for a 4-byte spill, which measured 2-6% faster.  Two blocks per slot need
 // their registers.
-template <int NBMAX, bool W16, int SPLIT>
+template <int NBMAX, bool W16, int SPLIT, bool NORM>
 __global__ void __launch_bounds__(kMaxThreads, NBMAX == 1 ? 3 : 1)
 prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restrict__ w_sf,
                       const float* __restrict__ tscale, int N, int K, int K_s, int nblocks, int S,
-                      void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale) {
+                      void* __restrict__ q, int f16_codes, int64_t ld_q, float* __restrict__ scale,
+                      float* __restrict__ norm) {
   extern __shared__ __align__(16) char smem[];
   float* red = reinterpret_cast<float*>(smem + S * kSlotBytes);
-  float* xred = red + kMaxThreads / 32;
+  float* xred = red + 16;
   const int slot = threadIdx.x >> 3, lane8 = threadIdx.x & 7;
   const float t16 = __ldg(tscale) * 0.0625f;  // t / 16 is exact
   const int row = blockIdx.x / SPLIT, part = blockIdx.x % SPLIT;
@@ -427,8 +474,8 @@ prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
   const int blk0 = part * nbl, nloc = min(nbl, nblocks - blk0);
   WRaw<NBMAX> r0;
   load_weight_row<NBMAX, W16>(w_fp4, w_sf, row, K, K_s, blk0, nloc, S, slot, lane8, r0);
-  weight_row<NBMAX, SPLIT>(r0, row, K, blk0, nloc, S, slot, lane8, t16, smem + slot * kSlotBytes, red, xred, q,
-                           f16_codes, ld_q, scale);
+  weight_row<NBMAX, SPLIT, NORM>(r0, row, K, blk0, nloc, S, slot, lane8, t16, smem + slot * kSlotBytes, red, xred, q,
+                           f16_codes, ld_q, scale, norm);
   if constexpr (SPLIT == 2) cluster_exit_wait();
 }
 
@@ -449,7 +496,7 @@ struct RowGeometry {
 // rows per SM than two blocks per slot: the activation rows gain from it
 // above 64 blocks, the shorter weight rows only where two blocks per slot
 // no longer fit one CTA (above 128).
-static bool row_geometry(int K_p, int split_above, RowGeometry* g) {
+[[maybe_unused]] static bool row_geometry(int K_p, int split_above, RowGeometry* g) {
   g->nblocks = K_p / kBlock;
   g->split = g->nblocks > split_above ? 2 : 1;
   const int nbl = (g->nblocks + g->split - 1) / g->split;
@@ -458,7 +505,7 @@ static bool row_geometry(int K_p, int split_above, RowGeometry* g) {
   g->nbmax = nb;
   g->S = (nbl + nb - 1) / nb;
   g->threads = ((kSlotThreads * g->S + 31) / 32) * 32;
-  g->smem = static_cast<size_t>(g->S) * kSlotBytes + (kMaxThreads / 32 + 4) * sizeof(float);
+  g->smem = static_cast<size_t>(g->S) * kSlotBytes + kRedFloats * sizeof(float);
   return true;
 }
 
@@ -492,67 +539,137 @@ static cudaError_t launch_rows(Kern k, const RowGeometry& g, int rows, cudaStrea
   return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
-template <int DT, bool SWIGLU, int VEC, int NB, int SPLIT>
+template <int DT, bool SWIGLU, int VEC, int NB, int SPLIT, bool NORM>
 static cudaError_t launch_act_cfg(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
-                                  const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
-  auto k = ps ? quant_act_kernel<DT, SWIGLU, NB, VEC, true, SPLIT>
-              : quant_act_kernel<DT, SWIGLU, NB, VEC, false, SPLIT>;
+                                  const float* ps, void* q, int f16, int64_t ld_q, float* scale, float* norm,
+                                  cudaStream_t st) {
   const int pf = prefetch_distance(static_cast<size_t>(SWIGLU ? 2 * K : K) * (DT == DT_FP32 ? 4 : 2));
-  return launch_rows(k, g, M, st, x, ld_x, M, K, g.nblocks, g.S, pf, ps, q, f16, ld_q, scale);
+  if constexpr (!SWIGLU && NB == 1 && SPLIT == 1) {
+    auto k = ps ? quant_act_kernel_r48<DT, VEC, true, NORM> : quant_act_kernel_r48<DT, VEC, false, NORM>;
+    return launch_rows(k, g, M, st, x, ld_x, M, K, g.nblocks, g.S, pf, ps, q, f16, ld_q, scale, norm);
+  } else {
+    auto k = ps ? quant_act_kernel<DT, SWIGLU, NB, VEC, true, SPLIT, NORM>
+                : quant_act_kernel<DT, SWIGLU, NB, VEC, false, SPLIT, NORM>;
+    return launch_rows(k, g, M, st, x, ld_x, M, K, g.nblocks, g.S, pf, ps, q, f16, ld_q, scale, norm);
+  }
 }
 
-template <int DT, bool SWIGLU, int VEC>
+template <int DT, bool SWIGLU, int VEC, bool NORM>
 static cudaError_t launch_act_dt(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
-                                 const float* ps, void* q, int f16, int64_t ld_q, float* scale, cudaStream_t st) {
-  if (g.split == 1) return launch_act_cfg<DT, SWIGLU, VEC, 1, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-  if (g.nbmax == 1) return launch_act_cfg<DT, SWIGLU, VEC, 1, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-  return launch_act_cfg<DT, SWIGLU, VEC, 2, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+                                 const float* ps, void* q, int f16, int64_t ld_q, float* scale, float* norm,
+                                 cudaStream_t st) {
+  if (g.split == 1)
+    return launch_act_cfg<DT, SWIGLU, VEC, 1, 1, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
+  if (g.nbmax == 1)
+    return launch_act_cfg<DT, SWIGLU, VEC, 1, 2, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
+  return launch_act_cfg<DT, SWIGLU, VEC, 2, 2, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
 }
 
-template <int DT>
+template <int DT, bool NORM>
 static cudaError_t launch_act(const RowGeometry& g, int M, const void* x, int64_t ld_x, int K,
                               bool swiglu, int vec, const float* ps, void* q, int f16, int64_t ld_q,
-                              float* scale, cudaStream_t st) {
+                              float* scale, float* norm, cudaStream_t st) {
   if (swiglu) {
     switch (vec) {
-      case 2: return launch_act_dt<DT, true, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-      case 1: return launch_act_dt<DT, true, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-      default: return launch_act_dt<DT, true, 0>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+      case 2: return launch_act_dt<DT, true, 2, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
+      case 1: return launch_act_dt<DT, true, 1, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
+      default: return launch_act_dt<DT, true, 0, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
     }
   }
   switch (vec) {
-    case 2: return launch_act_dt<DT, false, 2>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-    case 1: return launch_act_dt<DT, false, 1>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
-    default: return launch_act_dt<DT, false, 0>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, st);
+    case 2: return launch_act_dt<DT, false, 2, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
+    case 1: return launch_act_dt<DT, false, 1, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
+    default: return launch_act_dt<DT, false, 0, NORM>(g, M, x, ld_x, K, ps, q, f16, ld_q, scale, norm, st);
   }
 }
 
-template <bool W16, int NB, int SPLIT>
+template <bool W16, int NB, int SPLIT, bool NORM>
 static cudaError_t launch_weight_cfg(const RowGeometry& g, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
                                      const float* t, int K, int K_s, void* q, int f16, int64_t ld_q,
-                                     float* scale, cudaStream_t st) {
-  return launch_rows(prepare_weight_kernel<NB, W16, SPLIT>, g, N, st, w_fp4, w_sf, t, N, K, K_s, g.nblocks,
-                     g.S, q, f16, ld_q, scale);
+                                     float* scale, float* norm, cudaStream_t st) {
+  return launch_rows(prepare_weight_kernel<NB, W16, SPLIT, NORM>, g, N, st, w_fp4, w_sf, t, N, K, K_s, g.nblocks,
+                     g.S, q, f16, ld_q, scale, norm);
 }
 
-template <bool W16>
+template <bool W16, bool NORM>
 static cudaError_t launch_weight(const RowGeometry& g, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
                                  const float* t, int K, int K_s, void* q, int f16, int64_t ld_q, float* scale,
-                                 cudaStream_t st) {
+                                 float* norm, cudaStream_t st) {
   if (g.split == 1)
-    return g.nbmax == 1 ? launch_weight_cfg<W16, 1, 1>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st)
-                        : launch_weight_cfg<W16, 2, 1>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
-  if (g.nbmax == 1) return launch_weight_cfg<W16, 1, 2>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
-  return launch_weight_cfg<W16, 2, 2>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, st);
+    return g.nbmax == 1
+               ? launch_weight_cfg<W16, 1, 1, NORM>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st)
+               : launch_weight_cfg<W16, 2, 1, NORM>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st);
+  if (g.nbmax == 1)
+    return launch_weight_cfg<W16, 1, 2, NORM>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st);
+  return launch_weight_cfg<W16, 2, 2, NORM>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st);
 }
+
+// The launchers of the two objects this file compiles to: *_plain writes no
+// norm bounds, *_norm writes them to `norm`.
+cudaError_t launch_act_plain(const RowGeometry& g, int dt, int M, const void* x, int64_t ld_x, int K, bool swiglu,
+                             int vec, const float* ps, void* q, int f16, int64_t ld_q, float* scale, float* norm,
+                             cudaStream_t st);
+cudaError_t launch_act_norm(const RowGeometry& g, int dt, int M, const void* x, int64_t ld_x, int K, bool swiglu,
+                            int vec, const float* ps, void* q, int f16, int64_t ld_q, float* scale, float* norm,
+                            cudaStream_t st);
+cudaError_t launch_weight_plain(const RowGeometry& g, bool w16, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
+                                const float* t, int K, int K_s, void* q, int f16, int64_t ld_q, float* scale,
+                                float* norm, cudaStream_t st);
+cudaError_t launch_weight_norm(const RowGeometry& g, bool w16, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
+                               const float* t, int K, int K_s, void* q, int f16, int64_t ld_q, float* scale,
+                               float* norm, cudaStream_t st);
+
+template <bool NORM>
+static cudaError_t launch_act_any(const RowGeometry& g, int dt, int M, const void* x, int64_t ld_x, int K,
+                                  bool swiglu, int vec, const float* ps, void* q, int f16, int64_t ld_q,
+                                  float* scale, float* norm, cudaStream_t st) {
+  switch (dt) {
+    case DT_BF16: return launch_act<DT_BF16, NORM>(g, M, x, ld_x, K, swiglu, vec, ps, q, f16, ld_q, scale, norm, st);
+    case DT_FP16: return launch_act<DT_FP16, NORM>(g, M, x, ld_x, K, swiglu, vec, ps, q, f16, ld_q, scale, norm, st);
+    default: return launch_act<DT_FP32, NORM>(g, M, x, ld_x, K, swiglu, vec, ps, q, f16, ld_q, scale, norm, st);
+  }
+}
+
+template <bool NORM>
+static cudaError_t launch_weight_any(const RowGeometry& g, bool w16, int N, const uint8_t* w_fp4,
+                                     const uint8_t* w_sf, const float* t, int K, int K_s, void* q, int f16,
+                                     int64_t ld_q, float* scale, float* norm, cudaStream_t st) {
+  return w16 ? launch_weight<true, NORM>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st)
+             : launch_weight<false, NORM>(g, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st);
+}
+
+#if CONVROT_QUANT_NORM
+cudaError_t launch_act_norm(const RowGeometry& g, int dt, int M, const void* x, int64_t ld_x, int K, bool swiglu,
+                            int vec, const float* ps, void* q, int f16, int64_t ld_q, float* scale, float* norm,
+                            cudaStream_t st) {
+  return launch_act_any<true>(g, dt, M, x, ld_x, K, swiglu, vec, ps, q, f16, ld_q, scale, norm, st);
+}
+cudaError_t launch_weight_norm(const RowGeometry& g, bool w16, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
+                               const float* t, int K, int K_s, void* q, int f16, int64_t ld_q, float* scale,
+                               float* norm, cudaStream_t st) {
+  return launch_weight_any<true>(g, w16, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st);
+}
+#else
+cudaError_t launch_act_plain(const RowGeometry& g, int dt, int M, const void* x, int64_t ld_x, int K, bool swiglu,
+                             int vec, const float* ps, void* q, int f16, int64_t ld_q, float* scale, float* norm,
+                             cudaStream_t st) {
+  return launch_act_any<false>(g, dt, M, x, ld_x, K, swiglu, vec, ps, q, f16, ld_q, scale, norm, st);
+}
+cudaError_t launch_weight_plain(const RowGeometry& g, bool w16, int N, const uint8_t* w_fp4, const uint8_t* w_sf,
+                                const float* t, int K, int K_s, void* q, int f16, int64_t ld_q, float* scale,
+                                float* norm, cudaStream_t st) {
+  return launch_weight_any<false>(g, w16, N, w_fp4, w_sf, t, K, K_s, q, f16, ld_q, scale, norm, st);
+}
+#endif
 
 }  // namespace convrot
 
+#if !CONVROT_QUANT_NORM
 using namespace convrot;
 
 extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x, int M, int K,
                                  int swiglu, const float* pre_scale, void* a_q, convrot_codes fmt,
-                                 int64_t ld_aq, float* a_scale, cudaStream_t stream) {
+                                 int64_t ld_aq, float* a_scale, float* a_norm, cudaStream_t stream) {
   if (M < 0 || K <= 0) return CONVROT_ERR_INVALID_ARG;
   if (x_dtype != CONVROT_BF16 && x_dtype != CONVROT_FP16 && x_dtype != CONVROT_FP32)
     return CONVROT_ERR_UNSUPPORTED;
@@ -567,7 +684,8 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
   if (reinterpret_cast<uintptr_t>(x) % esize) return CONVROT_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(a_q) % (fmt == CONVROT_CODES_F16 ? 4 : 2) || ld_aq % 2)
     return CONVROT_ERR_MISALIGNED;
-  if (reinterpret_cast<uintptr_t>(a_scale) % 4 || reinterpret_cast<uintptr_t>(pre_scale) % 16)
+  if (reinterpret_cast<uintptr_t>(a_scale) % 4 || reinterpret_cast<uintptr_t>(pre_scale) % 16 ||
+      reinterpret_cast<uintptr_t>(a_norm) % 4)
     return CONVROT_ERR_MISALIGNED;
   // vector paths: every row start and the value half (SwiGLU) aligned to 32 or 16 bytes
   auto aligned = [&](int64_t a) {
@@ -578,18 +696,18 @@ extern "C" int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t l
   RowGeometry g;
   if (!row_geometry(K_p, kMaxSlots, &g)) return CONVROT_ERR_UNSUPPORTED;
   const int f16 = fmt == CONVROT_CODES_F16;
-  cudaError_t e;
-  switch (x_dtype) {
-    case CONVROT_BF16: e = launch_act<DT_BF16>(g, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, stream); break;
-    case CONVROT_FP16: e = launch_act<DT_FP16>(g, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, stream); break;
-    default: e = launch_act<DT_FP32>(g, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, stream); break;
-  }
+  const int dt = x_dtype == CONVROT_BF16 ? DT_BF16 : x_dtype == CONVROT_FP16 ? DT_FP16 : DT_FP32;
+  const cudaError_t e =
+      a_norm ? launch_act_norm(g, dt, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, a_norm,
+                               stream)
+             : launch_act_plain(g, dt, M, x, ld_x, K, swiglu != 0, vec, pre_scale, a_q, f16, ld_aq, a_scale, nullptr,
+                                stream);
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("quant_act launch", e);
 }
 
 extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
                                       const float* w_tensor_scale, int N, int K, void* w_q,
-                                      convrot_codes fmt, int64_t ld_wq, float* w_scale,
+                                      convrot_codes fmt, int64_t ld_wq, float* w_scale, float* w_norm,
                                       cudaStream_t stream) {
   if (N < 0 || K <= 0) return CONVROT_ERR_INVALID_ARG;
   if (fmt != CONVROT_CODES_S8 && fmt != CONVROT_CODES_F16) return CONVROT_ERR_UNSUPPORTED;
@@ -599,7 +717,7 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
   if (N == 0) return CONVROT_OK;
   if (!w_fp4 || !w_sf || !w_tensor_scale || !w_q || !w_scale) return CONVROT_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(w_fp4) % 8 || reinterpret_cast<uintptr_t>(w_tensor_scale) % 4 ||
-      reinterpret_cast<uintptr_t>(w_scale) % 4)
+      reinterpret_cast<uintptr_t>(w_scale) % 4 || reinterpret_cast<uintptr_t>(w_norm) % 4)
     return CONVROT_ERR_MISALIGNED;
   if (reinterpret_cast<uintptr_t>(w_q) % (fmt == CONVROT_CODES_F16 ? 4 : 2) || ld_wq % 2)
     return CONVROT_ERR_MISALIGNED;
@@ -607,11 +725,13 @@ extern "C" int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
   if (!row_geometry(K_p, 2 * kMaxSlots, &g)) return CONVROT_ERR_UNSUPPORTED;
   const int K_s = ((K + 15) / 16) * 16;
   const int f16 = fmt == CONVROT_CODES_F16;
-  cudaError_t e;
   // one 16-byte load per thread when every packed row starts 16-byte aligned
   const bool w16 = (reinterpret_cast<uintptr_t>(w_fp4) % 16 == 0) && ((K_s / 2) % 16 == 0);
-  e = w16 ? launch_weight<true>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream)
-          : launch_weight<false>(g, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, stream);
+  const cudaError_t e =
+      w_norm ? launch_weight_norm(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, w_norm,
+                                  stream)
+             : launch_weight_plain(g, w16, N, w_fp4, w_sf, w_tensor_scale, K, K_s, w_q, f16, ld_wq, w_scale, nullptr,
+                                   stream);
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("prepare_weight launch", e);
 }
 
@@ -661,3 +781,4 @@ extern "C" int convrot_widen_codes(const int8_t* src, int64_t ld_src, int rows, 
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? CONVROT_OK : convrot::record_cuda_error("widen_codes launch", e);
 }
+#endif  // !CONVROT_QUANT_NORM

@@ -55,6 +55,11 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
   return f2_of(d);
 }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)), "l"(u64_of(c)));
+  return f2_of(d);
+}
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   unsigned long long d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(u64_of(a)), "l"(u64_of(b)));
@@ -136,6 +141,17 @@ __device__ __forceinline__ float absmax_cols(float m, const BlockCols& c) {
   return m;
 }
 
+// Sum of squares of a block's 32 values held by this thread.
+__device__ __forceinline__ float sumsq_cols(float ss, const BlockCols& c) {
+  float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    a = fma2(c.U[p], c.U[p], a);
+    a = fma2(c.V[p], c.V[p], a);
+  }
+  return ss + (a.x + a.y);
+}
+
 __device__ __forceinline__ void scale_cols(BlockCols& c, float f) {
   const float2 ff = make_float2(f, f);
 #pragma unroll
@@ -169,6 +185,26 @@ struct RowQuant {
   __device__ __forceinline__ RowQuant(float s_, float r_) : s(s_), r(r_) {}
 };
 
+// Upper bound on the Euclidean norm of a row's codes, for the GEMM's choice
+// of exact FP32 chunk length.  The codes are q = clamp(rint(fp32(v * r)));
+// rounding moves each by at most 1/2 (plus the product's FP32 rounding,
+// below 127 * 2^-24) and the clamp only shrinks them, so
+// ||q|| <= r ||v|| + 0.5001 sqrt(K_p).  ||v|| = pre * sqrt(ss), ss being the
+// FP32 sum of squares of the values the quantiser saw before its `pre`
+// scaling; the factor 1 + 2^-10 covers that sum's rounding.  0 for a
+// degenerate row (all codes zero).
+__device__ __forceinline__ float code_norm_bound(const RowQuant& q, float ss, float pre, float half_sqrt_kp) {
+  if (q.s == 0.0f) return 0.0f;
+  return __fmaf_ru(sqrtf(ss) * (pre * q.r), 1.0f + 0.0009765625f, half_sqrt_kp);
+}
+
+// Sum over the warp (butterfly, every lane gets the total).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // Maximum over the warp of a non-negative float.  REDUX: non-negative floats
 // order like their bit patterns, so the integer warp reduction (one
 // instruction) applies; otherwise five shuffle-and-max steps.  Both give the
@@ -190,16 +226,29 @@ __device__ __forceinline__ float warp_max_nonneg(float v) {
 // reduces the per-warp maxima and computes s and r from amax * pre; every
 // thread reads them after a second barrier.  Cheaper than every warp
 // reducing the maxima and computing the division and the reciprocal itself.
-// `red` holds one float per warp plus s and r at [16], [17].
+// With with_ss, the row's sum of squares rides along and red[18] receives the
+// code-norm bound (uniform across the CTA: the caller asked for norms or not).
+// `red` layout (floats): [0, 16) per-warp maxima, [16] s, [17] r, [18] norm
+// bound, [24, 40) per-warp sums of squares.
+constexpr int kRedFloats = 48;
 template <bool REDUX>
-__device__ __forceinline__ RowQuant cta_rowquant(float local, float* red, float pre) {
+__device__ __forceinline__ RowQuant cta_rowquant(float local, float ss, bool with_ss, float* red, float pre,
+                                                 float half_sqrt_kp) {
   local = warp_max_nonneg<REDUX>(local);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  if (lane == 0) red[warp] = local;
+  if (with_ss) ss = warp_sum(ss);
+  if (lane == 0) {
+    red[warp] = local;
+    if (with_ss) red[24 + warp] = ss;
+  }
   __syncthreads();
   if (warp == 0) {
     const float m = warp_max_nonneg<REDUX>(lane < nwarps ? red[lane] : 0.f);
     const RowQuant q(m * pre);
+    if (with_ss) {
+      const float t = warp_sum(lane < nwarps ? red[24 + lane] : 0.f);
+      if (lane == 0) red[18] = code_norm_bound(q, t, pre, half_sqrt_kp);
+    }
     if (lane == 0) {
       red[16] = q.s;
       red[17] = q.r;
@@ -210,20 +259,30 @@ __device__ __forceinline__ RowQuant cta_rowquant(float local, float* red, float 
 }
 
 // The same for a row split over the two CTAs of a cluster: warp 0 reduces
-// this CTA's per-warp maxima and publishes the CTA maximum in xred[0]; after
-// a cluster barrier it reads the peer's, computes s and r and leaves them in
-// xred[2], xred[3] for the CTA.  Every thread of both CTAs must call it and
-// then call cluster_exit_wait() once before the CTA exits (the peer may read
-// xred[0] until then).
-__device__ __forceinline__ RowQuant cluster_rowquant(float local, float* red, float* xred, float pre) {
+// this CTA's per-warp maxima and sums of squares and publishes them in
+// xred[0], xred[1]; after a cluster barrier it reads the peer's, computes s,
+// r and the norm bound and leaves them in xred[2], xred[3], xred[4] for the
+// CTA.  Every thread of both CTAs must call it and then call
+// cluster_exit_wait() once before the CTA exits (the peer may read xred
+// until then).  xred = red + 16; the per-warp sums use red[24, 40).
+__device__ __forceinline__ RowQuant cluster_rowquant(float local, float ss, bool with_ss, float* red, float* xred,
+                                                     float pre, float half_sqrt_kp) {
   local = warp_max_nonneg<true>(local);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  if (lane == 0) red[warp] = local;
+  if (with_ss) ss = warp_sum(ss);
+  if (lane == 0) {
+    red[warp] = local;
+    if (with_ss) red[24 + warp] = ss;
+  }
   __syncthreads();
-  float m = 0.f;
+  float m = 0.f, t = 0.f;
   if (warp == 0) {
     m = warp_max_nonneg<true>(lane < nwarps ? red[lane] : 0.f);
-    if (lane == 0) xred[0] = m;
+    if (with_ss) t = warp_sum(lane < nwarps ? red[24 + lane] : 0.f);
+    if (lane == 0) {
+      xred[0] = m;
+      xred[1] = t;
+    }
   }
   __syncwarp();
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -232,12 +291,14 @@ __device__ __forceinline__ RowQuant cluster_rowquant(float local, float* red, fl
     const uint32_t local_addr = static_cast<uint32_t>(__cvta_generic_to_shared(xred));
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank ^ 1u));
-    float peer;
+    float peer, peer_ss;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(peer) : "r"(remote) : "memory");
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(peer_ss) : "r"(remote + 4) : "memory");
     const RowQuant q(fmaxf(m, peer) * pre);
     if (lane == 0) {
       xred[2] = q.s;
       xred[3] = q.r;
+      xred[4] = code_norm_bound(q, t + peer_ss, pre, half_sqrt_kp);
     }
   }
   __syncwarp();

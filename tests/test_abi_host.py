@@ -46,29 +46,31 @@ def test_status_strings(lib):
 def test_quant_act_rejects_bad_arguments(lib):
     f = lib.convrot_quant_act
     P = 1 << 20    # fake, never dereferenced: every call below fails validation first
-    assert f(P, 0, 512, 4, 0, 0, None, P, 1, 512, P, 0) == 1                 # K <= 0
-    assert f(P, 0, 512, -1, 512, 0, None, P, 1, 512, P, 0) == 1              # M < 0
-    assert f(P, 7, 512, 4, 512, 0, None, P, 1, 512, P, 0) == 3               # dtype
-    assert f(P, 0, 512, 4, 512, 0, None, P, 5, 512, P, 0) == 3               # code format
-    assert f(P, 0, 511, 4, 512, 0, None, P, 1, 512, P, 0) == 1               # ld_x < K
-    assert f(P, 0, 1023, 4, 512, 1, None, P, 1, 512, P, 0) == 1              # ld_x < 2K (SwiGLU)
-    assert f(P, 0, 512, 4, 300, 0, None, P, 1, 300, P, 0) == 1               # ld_aq < K_p
-    assert f(None, 0, 512, 4, 512, 0, None, P, 1, 512, P, 0) == 1            # null x
-    assert f(P + 1, 0, 512, 4, 512, 0, None, P, 1, 512, P, 0) == 2           # misaligned bf16
-    assert f(P, 0, 512, 4, 512, 0, P + 4, P, 1, 512, P, 0) == 2              # pre_scale not 16-byte aligned
-    assert f(P, 0, 70000, 4, 70000, 0, None, P, 1, 70144, P, 0) == 3         # K_p too large
-    assert f(P, 0, 512, 0, 512, 0, None, P, 1, 512, P, 0) == 0               # empty: no launch
+    assert f(P, 0, 512, 4, 0, 0, None, P, 1, 512, P, None, 0) == 1                 # K <= 0
+    assert f(P, 0, 512, -1, 512, 0, None, P, 1, 512, P, None, 0) == 1              # M < 0
+    assert f(P, 7, 512, 4, 512, 0, None, P, 1, 512, P, None, 0) == 3               # dtype
+    assert f(P, 0, 512, 4, 512, 0, None, P, 5, 512, P, None, 0) == 3               # code format
+    assert f(P, 0, 511, 4, 512, 0, None, P, 1, 512, P, None, 0) == 1               # ld_x < K
+    assert f(P, 0, 1023, 4, 512, 1, None, P, 1, 512, P, None, 0) == 1              # ld_x < 2K (SwiGLU)
+    assert f(P, 0, 512, 4, 300, 0, None, P, 1, 300, P, None, 0) == 1               # ld_aq < K_p
+    assert f(None, 0, 512, 4, 512, 0, None, P, 1, 512, P, None, 0) == 1            # null x
+    assert f(P + 1, 0, 512, 4, 512, 0, None, P, 1, 512, P, None, 0) == 2           # misaligned bf16
+    assert f(P, 0, 512, 4, 512, 0, P + 4, P, 1, 512, P, None, 0) == 2              # pre_scale not 16-byte aligned
+    assert f(P, 0, 70000, 4, 70000, 0, None, P, 1, 70144, P, None, 0) == 3         # K_p too large
+    assert f(P, 0, 512, 4, 512, 0, None, P, 1, 512, P, P + 2, 0) == 2        # a_norm misaligned
+    assert f(P, 0, 512, 0, 512, 0, None, P, 1, 512, P, None, 0) == 0               # empty: no launch
 
 
 def test_prepare_weight_rejects_bad_arguments(lib):
     f = lib.convrot_prepare_weight
     P = 1 << 20
-    assert f(P, P, P, 4, 0, P, 1, 512, P, 0) == 1                      # K <= 0
-    assert f(P, P, P, 4, 512, P, 1, 256, P, 0) == 1                    # ld_wq < K_p
-    assert f(P + 4, P, P, 4, 512, P, 1, 512, P, 0) == 2                # w_fp4 not 8-aligned
-    assert f(P, P, P, 4, 512, P + 1, 1, 512, P, 0) == 2                # f16 codes misaligned
-    assert f(P, None, P, 4, 512, P, 1, 512, P, 0) == 1                 # null scales
-    assert f(P, P, P, 0, 512, P, 1, 512, P, 0) == 0                    # empty
+    assert f(P, P, P, 4, 0, P, 1, 512, P, None, 0) == 1                      # K <= 0
+    assert f(P, P, P, 4, 512, P, 1, 256, P, None, 0) == 1                    # ld_wq < K_p
+    assert f(P + 4, P, P, 4, 512, P, 1, 512, P, None, 0) == 2                # w_fp4 not 8-aligned
+    assert f(P, P, P, 4, 512, P + 1, 1, 512, P, None, 0) == 2                # f16 codes misaligned
+    assert f(P, None, P, 4, 512, P, 1, 512, P, None, 0) == 1                 # null scales
+    assert f(P, P, P, 4, 512, P, 1, 512, P, P + 1, 0) == 2             # w_norm misaligned
+    assert f(P, P, P, 0, 512, P, 1, 512, P, None, 0) == 0                    # empty
 
 
 def test_gemm_rejects_bad_arguments(lib):
@@ -78,8 +80,8 @@ def test_gemm_rejects_bad_arguments(lib):
 
     def call(**kw):
         d = dict(ok, **kw)
-        return f(d["a"], d["lda"], d["sa"], d["w"], d["ldw"], d["sw"], d.get("b"), d["M"], d["N"],
-                 d["Kp"], d["o"], d["dt"], d["ldo"], 0)
+        return f(d["a"], d["lda"], d["sa"], d.get("an"), d["w"], d["ldw"], d["sw"], d.get("wn"), d.get("b"),
+                 d["M"], d["N"], d["Kp"], d["o"], d["dt"], d["ldo"], 0)
     assert call(Kp=500) == 1                 # K_p not a multiple of 256
     assert call(Kp=0) == 1
     assert call(lda=256) == 1                # ld < K_p
@@ -92,9 +94,11 @@ def test_gemm_rejects_bad_arguments(lib):
     assert call(M=0) == 0 and call(N=0) == 0
     assert call(sw=P + 4) == 2               # w_scale read four at a time
     assert call(b=P + 4) == 2                # bias read four at a time
+    assert call(an=P + 2, wn=P) == 2         # norm bounds 4-byte aligned
     g = lib.convrot_gemm_i32
-    assert g(P, 512, P, 512, 4, 4, 512, None, 4, 0) == 1
-    assert g(P, 512, P, 512, 4, 4, 512, P + 2, 4, 0) == 2
+    assert g(P, 512, None, P, 512, None, 4, 4, 512, None, 4, 0) == 1
+    assert g(P, 512, None, P, 512, None, 4, 4, 512, P + 2, 4, 0) == 2
+    assert g(P, 512, P + 1, P, 512, P, 4, 4, 512, P, 4, 0) == 2
 
 
 def test_binding_fails_loudly_without_library(tmp_path):

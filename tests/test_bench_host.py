@@ -21,8 +21,9 @@ def test_qkv_algorithmic_counts():
     # packed NVFP4 + E4M3 scales once, one-byte codes once, one FP32 scale per row
     assert sz["w_alg"] == N * K // 2 + N * K // 16 + N * K + 4 * N == 180719616
     # bytes moved with the codes held as FP16 for the GEMM (and the tensor scale read)
-    assert sz["act_bytes"] == M * K * 2 + M * K * 2 + 4 * M == 429923412
-    assert sz["w_bytes"] == N * K // 2 + N * K // 16 + 4 + N * K * 2 + 4 * N == 296325124
+    # QKV (K_p = 5376) asks for the code-norm bounds: 4 more bytes per row
+    assert sz["act_bytes"] == M * K * 2 + M * K * 2 + 8 * M == 430003368
+    assert sz["w_bytes"] == N * K // 2 + N * K // 16 + 4 + N * K * 2 + 8 * N == 296411140
     assert sz["gemm_flops"] == 2.0 * M * N * K
     assert abs(sz["gemm_flops"] - 4.6217e12) / 4.6217e12 < 1e-4
 
@@ -75,3 +76,9 @@ def test_reference_arm_shares_the_workload_config():
     c = bench.bench_config(wl, 0)
     assert c["workload"] == "qkv M=19989 K=5376 N=21504 bf16->bf16"
     assert c == bench.bench_config(wl, 0)
+
+
+def test_norm_bounds_requested_where_they_can_pay():
+    # QKV / FFN-up (K_p = 5376) ask for them; FFN-down (14336) and wide K do not
+    assert bench.norms_pay(5376) and bench.norms_pay(8192)
+    assert not bench.norms_pay(14336) and not bench.norms_pay(20480)

@@ -330,8 +330,8 @@ def test_empty_calls_launch_nothing():
     import rotated_w4a8_int8_gb300 as cr
     lib = cr.load_library()
     y = torch.full((4, 4), 3.0, device=DEV)
-    assert lib.convrot_gemm(16, 512, 16, 16, 512, 16, None, 0, 4, 512, y.data_ptr(), 2, 4, 0) == 0
-    assert lib.convrot_quant_act(16, 0, 512, 0, 512, 0, None, 16, 1, 512, 16, 0) == 0
+    assert lib.convrot_gemm(16, 512, 16, None, 16, 512, 16, None, None, 0, 4, 512, y.data_ptr(), 2, 4, 0) == 0
+    assert lib.convrot_quant_act(16, 0, 512, 0, 512, 0, None, 16, 1, 512, 16, None, 0) == 0
     torch.cuda.synchronize()
     assert torch.all(y == 3.0)
 
