@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from an ncu capture of
 # this kernel; valid only while code_sha16(gemm.cu) equals this (the hash ignores comments;
 # otherwise the bench line reports traffic as null).
-GEMM_TRAFFIC = {"sha256_16": "b3110dca79e8ac91", "bytes": 2818213120 + 848316160}
+GEMM_TRAFFIC = {"sha256_16": "87675c6ec0e37096", "bytes": 2987120896 + 849276672}
 
 
 def code_sha16(path: str) -> str:
@@ -359,6 +359,7 @@ class E2EPipeline:
         out_done = [None, None]      # output of the buffer copied out (y free)
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        marks = []                   # each step's output copied out (timing events)
         t0.record(self.s_in)
         for i in range(steps):
             b = self.bufs[i % 2]
@@ -400,6 +401,8 @@ class E2EPipeline:
                     self.s_out.wait_stream(sp)
                 out_done[k] = ev()
                 out_done[k].record(self.s_out)
+                marks.append(torch.cuda.Event(enable_timing=True))
+                marks[-1].record(self.s_out)
         self.s_out.wait_stream(self.s_in)
         self.s_out.wait_stream(self.s_run)
         t1.record(self.s_out)
@@ -407,6 +410,8 @@ class E2EPipeline:
             while not t1.query():
                 pass
         t1.synchronize()
+        # intervals between consecutive steps' output completions
+        self.step_ms = [marks[i - 1].elapsed_time(marks[i]) for i in range(1, len(marks))]
         return t0.elapsed_time(t1)
 
 
@@ -485,7 +490,12 @@ def time_e2e(layer: Layer, steps: int, warmup: int, world: int):
     ms = pipe.run(steps)
     torch.cuda.synchronize()
     barrier(world)
-    return ms, pipe.in_bytes, pipe.out_bytes, link
+    iv = sorted(pipe.step_ms)
+    intervals = None
+    if iv:
+        intervals = {"min": iv[0], "median": iv[len(iv) // 2], "max": iv[-1],
+                     "first": pipe.step_ms[0], "last": pipe.step_ms[-1]}
+    return ms, pipe.in_bytes, pipe.out_bytes, link, intervals
 
 
 def time_ffn_block(dev, world, flush, warmup, steps=10):
@@ -883,11 +893,11 @@ def main():
                       "note": "lower bound on a decode-inside-GEMM layer from this run's weight-kernel time"}
 
     # end-to-end through the public API with host buffers
-    e2e_value = e2e_ms = link = None
+    e2e_value = e2e_ms = link = intervals = None
     h2d = layer.in_bytes
     d2h = layer.y.numel() * layer.y.element_size()
     if args.e2e_steps > 0:
-        e2e_ms, h2d, d2h, link = time_e2e(layer, args.e2e_steps, 3, 1)
+        e2e_ms, h2d, d2h, link, intervals = time_e2e(layer, args.e2e_steps, 3, 1)
         e2e_value = aggregate_tops(sz["ops"], args.e2e_steps, e2e_ms, 1)
     sustained = None
     if args.sustained_s > 0:
@@ -982,7 +992,10 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "pipelined": "streams: copy-in, kernels, copy-out split over 2 copy streams",
                 "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None,
-                "host_link_gbs": link},
+                "host_link_gbs": link,
+                # time between consecutive steps' output completions: a slow box shows here
+                # whether every step or a few are slow
+                "step_interval_ms": intervals},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "sustained": sustained,
