@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from an ncu capture of
 # this kernel; valid only while code_sha16(gemm.cu) equals this (the hash ignores comments;
 # otherwise the bench line reports traffic as null).
-GEMM_TRAFFIC = {"sha256_16": "87675c6ec0e37096", "bytes": 2987120896 + 849276672}
+GEMM_TRAFFIC = {"sha256_16": "8ddb182916d20b04", "bytes": 3027598848 + 936688384}
 
 
 def code_sha16(path: str) -> str:
@@ -480,22 +480,32 @@ def host_link_gbs(pipe: "E2EPipeline", reps: int = 3):
     return out
 
 
-def time_e2e(layer: Layer, steps: int, warmup: int, world: int):
+def time_e2e(layer: Layer, steps: int, warmup: int, world: int, runs: int = 3):
+    """`runs` timed runs of `steps` pipelined steps; returns the median run's
+    time and per-step intervals, and every run's ms per step.  On some boxes a
+    single step of a run stalled for tens of milliseconds (its neighbours at
+    the usual 4.4-4.6 ms), so one run alone can misstate the pipeline."""
     import torch
     pipe = E2EPipeline(layer)
     pipe.run(warmup)
     torch.cuda.synchronize()
     link = host_link_gbs(pipe)
-    barrier(world)
-    ms = pipe.run(steps)
-    torch.cuda.synchronize()
-    barrier(world)
-    iv = sorted(pipe.step_ms)
+    results = []
+    for _ in range(runs):
+        barrier(world)
+        ms = pipe.run(steps)
+        torch.cuda.synchronize()
+        barrier(world)
+        results.append((ms, list(pipe.step_ms)))
+    order = sorted(range(runs), key=lambda r: results[r][0])
+    ms, step_ms = results[order[runs // 2]]
+    iv = sorted(step_ms)
     intervals = None
     if iv:
         intervals = {"min": iv[0], "median": iv[len(iv) // 2], "max": iv[-1],
-                     "first": pipe.step_ms[0], "last": pipe.step_ms[-1]}
-    return ms, pipe.in_bytes, pipe.out_bytes, link, intervals
+                     "first": step_ms[0], "last": step_ms[-1]}
+    runs_ms_per_step = [r[0] / steps for r in results]
+    return ms, pipe.in_bytes, pipe.out_bytes, link, intervals, runs_ms_per_step
 
 
 def time_ffn_block(dev, world, flush, warmup, steps=10):
@@ -893,11 +903,11 @@ def main():
                       "note": "lower bound on a decode-inside-GEMM layer from this run's weight-kernel time"}
 
     # end-to-end through the public API with host buffers
-    e2e_value = e2e_ms = link = intervals = None
+    e2e_value = e2e_ms = link = intervals = e2e_runs = None
     h2d = layer.in_bytes
     d2h = layer.y.numel() * layer.y.element_size()
     if args.e2e_steps > 0:
-        e2e_ms, h2d, d2h, link, intervals = time_e2e(layer, args.e2e_steps, 3, 1)
+        e2e_ms, h2d, d2h, link, intervals, e2e_runs = time_e2e(layer, args.e2e_steps, 3, 1)
         e2e_value = aggregate_tops(sz["ops"], args.e2e_steps, e2e_ms, 1)
     sustained = None
     if args.sustained_s > 0:
@@ -992,6 +1002,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "pipelined": "streams: copy-in, kernels, copy-out split over 2 copy streams",
                 "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None,
+                "statistic": "median of 3 timed runs of e2e_steps pipelined steps",
+                "runs_ms_per_step": e2e_runs,
                 "host_link_gbs": link,
                 # time between consecutive steps' output completions: a slow box shows here
                 # whether every step or a few are slow

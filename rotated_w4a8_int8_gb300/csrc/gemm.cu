@@ -621,6 +621,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         // shadow of this item's first accumulator (measured free)
         nchunks = tile_chunks(p, m2, nt, lane, chunks_per_tile);
       }
+      // One chunk (dequantised outputs): the FP32 accumulator already is the
+      // exact integer sum (below 2^24), so acc keeps its bits, with no
+      // conversion.  Several chunks (or int32 output): each chunk is converted
+      // to int32 (exact) and added; for dequantised outputs the total is
+      // turned into FP32 bits once at the end.  The FP32 value either way is
+      // fp32(sum), rounded to nearest.
+      const bool keep_bits = OUT >= 0 && nchunks == 1;
       int32_t acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0;
@@ -635,15 +642,26 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         const uint32_t t_base = tmem_base + lane_addr + buf * BN + col_half * 128;
         // 16 columns per load: with 32, the 128 int32 accumulators and the
         // load's registers exceed the 168-register budget and spill
+        if (keep_bits) {
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(t_base + g * 16, r);
-          tmem_ld_wait();
+          for (int g = 0; g < 8; ++g) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(t_base + g * 16, r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            // the FP32 value is an exact integer below 2^24: conversion is exact
-            acc[g * 16 + j] += __float2int_rn(__uint_as_float(r[j]));
+            for (int j = 0; j < 16; ++j) acc[g * 16 + j] = static_cast<int32_t>(r[j]);
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            uint32_t r[16];
+            tmem_ld_32x32b_x16(t_base + g * 16, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              // the FP32 value is an exact integer below 2^24: conversion is exact
+              acc[g * 16 + j] += __float2int_rn(__uint_as_float(r[j]));
+            }
           }
         }
         tc_fence_before();
@@ -651,6 +669,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         if (lane == 0) mbar_arrive_cluster(lacce0 + 8 * buf);
       }
       if (!ok) break;
+      if (OUT >= 0 && !keep_bits) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = __float_as_int(static_cast<float>(acc[j]));
+      }
       // ---- output: this thread owns row m, columns n0 .. n0+127
       const int m_base = mb * BM + quarter * 32;
       const int m = m_base + lane;
@@ -710,7 +732,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
               float yv[VEC];
 #pragma unroll
               for (int q = 0; q < VEC; ++q) {
-                const float y = __fmul_rn(__fmul_rn(static_cast<float>(acc[j0 + q]), sa), sw[q]);
+                const float y = __fmul_rn(__fmul_rn(__int_as_float(acc[j0 + q]), sa), sw[q]);
                 yv[q] = BIAS ? __fadd_rn(y, bs[q]) : y;
               }
               if constexpr (sizeof(T) == 2) {
