@@ -186,3 +186,62 @@ def test_mixed_items_and_ring_reuse():
     assert big * big >= LIMIT and big * np.sqrt(np.sum(qw[:256].astype(np.float64) ** 2, axis=1)).max() < LIMIT
     ref = oracle.int_gemm(qa, qw)
     assert np.array_equal(run_i32(qa, qw, True), ref)
+
+
+@pytest.mark.parametrize("t", [-3.7, 1e-6, 2.0e4])
+def test_weight_bounds_hold_on_random_nvfp4_bytes(t):
+    # any stored bytes (all 16 E2M1 codes, random non-NaN E4M3 scales with
+    # subnormals and sign bits) and tensor scales of either sign and far from
+    # 1: the bound comes from the decoded row before the rotation, scaled by |t|
+    import rotated_w4a8_int8_gb300 as cr
+    rng = np.random.default_rng(23)
+    N, K = 64, 5000
+    Ks = (K + 15) // 16 * 16
+    Kp = oracle.padded_k(K)
+    packed = rng.integers(0, 256, (N, Ks // 2), dtype=np.uint8)
+    scales = rng.integers(0, 256, (N, Ks // 16), dtype=np.uint8)
+    scales[(scales & 0x7F) == 0x7F] = 0x38                  # no NaN scale bytes
+    q = torch.empty(N, Kp, dtype=torch.float16, device=DEV)
+    s = torch.empty(N, dtype=torch.float32, device=DEV)
+    nrm = torch.full((N,), -1.0, dtype=torch.float32, device=DEV)
+    cr.prepare_weight(torch.from_numpy(packed).to(DEV), torch.from_numpy(scales).to(DEV),
+                      torch.tensor([t], dtype=torch.float32, device=DEV), K, q, s, w_norm=nrm)
+    check_bounds(codes_to_np(q, Kp), nrm.cpu().numpy(), Kp)
+
+
+CODE_CASES = [small("qkv", 64, 8), small("ffn_down", 48, 8), small("wide_k", 16, 8),
+              synth.Workload("pre", 40, 3000, 8, "bf16", "bf16", False, 0.0, 1.0, 41),
+              synth.Workload("swpre", 40, 3000, 8, "bf16", "bf16", True, 0.0, 1.0, 43)]
+
+
+@pytest.mark.parametrize("wl", CODE_CASES, ids=[w.name for w in CODE_CASES])
+def test_codes_do_not_depend_on_asking_for_bounds(wl):
+    # the bounds are a side result: codes and scales are bit-identical with and
+    # without them (SwiGLU, channel pre-scales, split rows, and the weights)
+    import rotated_w4a8_int8_gb300 as cr
+    Kp = oracle.padded_k(wl.K)
+    x = storage_to_dev(synth.make_activations(wl), wl.x_dtype)
+    pre = None
+    if wl.name in ("pre", "swpre"):
+        gen = torch.Generator(device="cpu").manual_seed(5)
+        pre = torch.exp(torch.rand(wl.K, generator=gen) * 2 - 1).to(DEV)
+    outs = []
+    for with_norm in (False, True):
+        q = torch.empty(wl.M, Kp, dtype=torch.float16, device=DEV)
+        s = torch.empty(wl.M, dtype=torch.float32, device=DEV)
+        nrm = torch.empty(wl.M, dtype=torch.float32, device=DEV) if with_norm else None
+        cr.quant_act(x, wl.K, q, s, swiglu=wl.swiglu, pre_scale=pre, a_norm=nrm)
+        outs.append((q, s))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    ww = small(wl.name if wl.name in synth.WORKLOADS else "qkv", 8, 40)   # 40 weight rows, the same K
+    packed, scales, t = synth.make_nvfp4_weight(ww)
+    Kpw = oracle.padded_k(ww.K)
+    wouts = []
+    for with_norm in (False, True):
+        q = torch.empty(ww.N, Kpw, dtype=torch.float16, device=DEV)
+        s = torch.empty(ww.N, dtype=torch.float32, device=DEV)
+        nrm = torch.empty(ww.N, dtype=torch.float32, device=DEV) if with_norm else None
+        cr.prepare_weight(torch.from_numpy(packed).to(DEV), torch.from_numpy(scales).to(DEV),
+                          torch.tensor([float(t)], dtype=torch.float32, device=DEV), ww.K, q, s, w_norm=nrm)
+        wouts.append((q, s))
+    assert torch.equal(wouts[0][0], wouts[1][0]) and torch.equal(wouts[0][1], wouts[1][1])
