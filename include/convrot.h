@@ -37,8 +37,10 @@
  * (CONVROT_CODES_F16, two bytes per code).  convrot_gemm reads the FP16
  * form: sm_103a tensor cores have no 8-bit integer MMA, so the GEMM runs the
  * FP16 tensor-core path, whose FP32 accumulation of these integer products
- * is exact, and it converts to int32 every 1024 K.  The int32 accumulator is
- * therefore bit-exact.
+ * is exact while partial sums stay below 2^24: it converts to int32 every
+ * 1024 K, or once per output tile when the rows' code-norm bounds show that
+ * no partial sum can reach 2^24.  The int32 accumulator is therefore
+ * bit-exact either way.
  */
 #ifndef CONVROT_H
 #define CONVROT_H
@@ -82,7 +84,8 @@ const char* convrot_status_string(int status);
  *
  * Row ranges: the call has no row-offset argument.  To prepare rows
  * [n0, n0 + n) of a weight, pass w_fp4 + n0 * (K_s/2), w_sf + n0 * (K_s/16),
- * w_q + n0 * ld_wq (in code elements) and w_scale + n0 with N = n; rows are
+ * w_q + n0 * ld_wq (in code elements), w_scale + n0 and (if used)
+ * w_norm + n0 with N = n; rows are
  * independent, so the result equals that of the whole-weight call (the
  * alignment rules below apply to the offset pointers).
  *
@@ -162,7 +165,8 @@ int convrot_quant_act(const void* x, convrot_dtype x_dtype, int64_t ld_x,
  *   w_q     [N][ld_wq] FP16-stored S8 codes of the rotated weights.
  *   a_scale [M], w_scale [N] FP32 row scales (w_scale 16-byte aligned).
  *   a_norm, w_norm  NULL, or the [M] and [N] code-norm bounds written by
- *           convrot_quant_act and convrot_prepare_weight (4-byte aligned).
+ *           convrot_quant_act and convrot_prepare_weight (4-byte aligned;
+ *           both are needed, one alone is ignored).
  *           The tensor cores accumulate in FP32, so the int32 result is exact
  *           only while every partial sum stays below 2^24.  Without the
  *           bounds the K loop is cut into exact chunks of at most 1024
