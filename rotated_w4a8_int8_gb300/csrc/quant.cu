@@ -352,11 +352,13 @@ quant_act_kernel(const void* __restrict__ x, int64_t ld_x, int M, int K, int nbl
 }
 
 // The plain single-CTA form (no SwiGLU, one block per slot) held to 48
-// registers: 7 CTAs of a 21-block row then fit an SM instead of 6 (QKV
-// activations 76.5 -> 74.4 us, same box, alternating order; 42 registers,
-// 8 CTAs, measured slower; with the norm bound's sum of squares 86.7 -> 84.3
-// us).  The other forms keep the 512-thread launch bound alone: held to 48
-// registers, the SwiGLU form spills and ran 25% slower.
+// registers measured faster: QKV activations 76.5 -> 74.4 us (same box,
+// alternating order; 42 registers measured slower), and 86.7 -> 84.3 us with
+// the norm bound's sum of squares.  ncu reports the same register limit (6
+// CTAs of a 21-block row per SM) for the 48-register form, so the gain is in
+// the schedule, not the occupancy.  The other forms keep the 512-thread
+// launch bound alone: held to 48 registers, the SwiGLU form spills and ran
+// 25% slower.
 template <int DT, int VEC, bool PRESCALE, bool NORM>
 __global__ void __maxnreg__(48)
 quant_act_kernel_r48(const void* __restrict__ x, int64_t ld_x, int M, int K, int nblocks, int S, int pf_dist,
@@ -489,8 +491,8 @@ prepare_weight_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
 }
 
 // Short rows (at most kShortRowBlocks blocks, one per slot) held to 48
-// registers instead: 7 CTAs of a 21-block row per SM, no spill, and a freer
-// schedule.  Measured on one box (alternating order): 21-block rows 82.1 ->
+// registers instead: no spill (ncu: 6 CTAs of a 21-block row per SM by
+// registers).  Measured on one box (alternating order): 21-block rows 82.1 ->
 // 76.4 us, and 91.9 -> 88.7 us with the norm bound's sum of squares (which
 // spills at 40 registers); on 56-block rows the 48-register form was even
 // (62.1 -> 62.8 us) and, with the sum of squares, 13% slower, so longer rows
