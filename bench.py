@@ -642,7 +642,10 @@ def time_library_controls(layer: "Layer", flush, warmup, steps=20):
     - int8_mm: torch._int_mm (cuBLASLt S8 x S8 -> int32) on the same codes as
       int8, and on random codes at 8192^3: the rate of the S8 tensor path
       this GPU offers through the library, the denominator of an "INT8
-      roofline"."""
+      roofline";
+    - int8_mma_sync: this library's register-resident probe of the
+      warp-level INT8 tensor instruction (mma.sync m16n8k32 s8) on every SM,
+      the hardware side of the same denominator."""
     import torch
     A, B = layer.aq, layer.wq
     M, Kp = A.shape
@@ -685,6 +688,26 @@ def time_library_controls(layer: "Layer", flush, warmup, steps=20):
         except RuntimeError as e:            # not offered by this torch build
             out[name] = {"shape": f"{m}x{n}x{k}", "unavailable": str(e).splitlines()[0][:200]}
         torch.cuda.empty_cache()
+    # 8 CTAs of 4 warps per SM, 8 independent MMAs per warp and iteration
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = 8 * sms, 20000
+    res = torch.empty(blocks * 4, dtype=torch.int32, device=dev)
+    layer.cr.int8_mma_probe(blocks, 100, res)
+    best = None
+    for _ in range(5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        layer.cr.int8_mma_probe(blocks, iters, res)
+        b.record()
+        b.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    if not bool((res == 8 * 32 * iters).all()):
+        raise RuntimeError("INT8 MMA probe returned wrong sums")
+    ops = blocks * 4 * iters * 8 * (2 * 16 * 8 * 32)
+    out["int8_mma_sync"] = {"what": "mma.sync.m16n8k32 s8 x s8 -> s32 from registers, 8 CTAs of 4 warps per SM, "
+                                    "best of 5 launches", "ms": best, "tops": ops / (best / 1e3) / 1e12}
     return out
 
 
@@ -984,6 +1007,10 @@ def main():
     if library and "tops" in library.get("int8_mm", {}):
         roofline["int8_library_tops_same_shape"] = library["int8_mm"]["tops"]
         roofline["vs_int8_library_same_shape"] = achieved / library["int8_mm"]["tops"]
+    if library and "tops" in library.get("int8_mma_sync", {}):
+        # the INT8 tensor rate of this GPU measured on the warp-level instruction
+        roofline["int8_mma_sync_tops"] = library["int8_mma_sync"]["tops"]
+        roofline["vs_int8_mma_sync"] = achieved / library["int8_mma_sync"]["tops"]
 
     line = {
         "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": 1, "steps": args.steps,

@@ -235,6 +235,18 @@ int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq,
                                   int32_t* acc, int64_t ld_acc, cudaStream_t stream);
 
 /*
+ * Measurement aid, not part of the layer (the pages have no counterpart): runs
+ * the warp-level INT8 tensor instruction (mma.sync m16n8k32, s8 x s8 -> s32)
+ * from registers, `blocks` CTAs of 4 warps, each warp issuing 8 independent
+ * MMAs per iteration for `iters` iterations (2 * 16 * 8 * 32 = 8192 integer
+ * operations per MMA).  Every operand byte is 1, so each warp writes
+ * 8 * 32 * iters to out[warp] (out: blocks * 4 int32, device).  Timing the
+ * call gives this GPU's INT8 rate on that path, the denominator of "% of
+ * INT8 roofline".  iters in [1, 2^22].
+ */
+int convrot_int8_mma_probe(int blocks, int iters, int32_t* out, cudaStream_t stream);
+
+/*
  * Text of the last CUDA error that made a call of this library return
  * CONVROT_ERR_CUDA in the calling thread, naming the failing CUDA call
  * ("" if none).  The string is owned by the library and stays valid until

@@ -14,7 +14,8 @@ import os
 
 __all__ = [
     "load_library", "padded_k", "status_string", "last_error", "prepare_weight", "quant_act", "gemm",
-    "gemm_i32", "widen_codes", "gemm_timeout_selftest", "device_error", "ConvRotError", "BF16", "FP16", "FP32", "CODES_S8",
+    "gemm_i32", "widen_codes", "gemm_timeout_selftest", "int8_mma_probe", "device_error", "ConvRotError", "BF16", "FP16",
+    "FP32", "CODES_S8",
     "CODES_F16", "LIB_PATH", "EXPORTS",
 ]
 
@@ -23,7 +24,7 @@ BF16, FP16, FP32 = 0, 1, 2
 CODES_S8, CODES_F16 = 0, 1
 EXPORTS = ("convrot_padded_k", "convrot_status_string", "convrot_prepare_weight",
            "convrot_quant_act", "convrot_gemm", "convrot_gemm_i32", "convrot_device_error",
-           "convrot_last_error", "convrot_gemm_timeout_selftest", "convrot_widen_codes")
+           "convrot_last_error", "convrot_gemm_timeout_selftest", "convrot_widen_codes", "convrot_int8_mma_probe")
 
 _lib = None
 
@@ -61,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.convrot_widen_codes.restype = i32
     lib.convrot_gemm_timeout_selftest.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp, i64, vp]
     lib.convrot_gemm_timeout_selftest.restype = i32
+    lib.convrot_int8_mma_probe.argtypes = [i32, i32, vp, vp]
+    lib.convrot_int8_mma_probe.restype = i32
     lib.convrot_last_error.argtypes = []
     lib.convrot_last_error.restype = ctypes.c_char_p
     lib.convrot_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -174,6 +177,12 @@ def gemm_timeout_selftest(a_q, w_q, acc, K_p: int | None = None, stream=None) ->
     _check("convrot_gemm_timeout_selftest", load_library().convrot_gemm_timeout_selftest(
         _ptr(a_q), _ld(a_q), _ptr(w_q), _ld(w_q), M, N, int(K_p), _ptr(acc),
         _ld(acc), _stream(stream)))
+
+
+def int8_mma_probe(blocks: int, iters: int, out, stream=None) -> None:
+    """convrot_int8_mma_probe: out int32 [blocks * 4]; each entry becomes 8 * 32 * iters."""
+    _check("convrot_int8_mma_probe", load_library().convrot_int8_mma_probe(
+        int(blocks), int(iters), _ptr(out), _stream(stream)))
 
 
 def device_error(stream=None) -> int:

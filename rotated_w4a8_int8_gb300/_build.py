@@ -19,7 +19,8 @@ LIB = os.path.join(HERE, "libconvrot.so")
 # (source, object, defines): quant.cu is compiled twice, once without and once
 # with the kernels that write code-norm bounds
 SOURCES = [("api.cu", "api", []), ("quant.cu", "quant", []),
-           ("quant.cu", "quant_norm", ["-DCONVROT_QUANT_NORM=1"]), ("gemm.cu", "gemm", [])]
+           ("quant.cu", "quant_norm", ["-DCONVROT_QUANT_NORM=1"]), ("gemm.cu", "gemm", []),
+           ("int8_probe.cu", "int8_probe", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -131,3 +131,13 @@ def test_single_row_tensors_pass_their_width_as_pitch():
     assert t.stride(0) in (0, 512)
     assert cr._ld(t) == 512
     assert cr._ld(torch.zeros(3, 40)[:, :16]) == 40
+
+
+def test_int8_probe_rejects_bad_arguments(lib):
+    f = lib.convrot_int8_mma_probe
+    P = 1 << 20
+    assert f(0, 10, P, 0) == 1                      # no blocks
+    assert f(4, 0, P, 0) == 1                       # no iterations
+    assert f(4, (1 << 22) + 1, P, 0) == 1           # the per-warp sum would overflow int32
+    assert f(4, 10, None, 0) == 1
+    assert f(4, 10, P + 2, 0) == 2                  # int32 output misaligned
