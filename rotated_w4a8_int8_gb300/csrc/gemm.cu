@@ -16,12 +16,13 @@
 // kind::f16 with FP32 accumulation in tensor memory.  Products are at most
 // 127^2 and a 1024-deep partial sum at most 127^2 * 1024 = 16,516,096 < 2^24,
 // so every FP32 partial sum is an exact integer (tests drive running sums
-// that are odd and above 2^23).  The K loop is therefore cut into 1024-wide
-// chunks, each accumulated afresh in one of two TMEM buffers; epilogue warps
-// convert each finished chunk to int32 (exact) and add it to per-thread int32
-// registers while the tensor core fills the other buffer.  Given bounds on
-// the rows' code norms, a work item whose bounds keep every partial sum
-// below 2^24 (Cauchy-Schwarz) runs its whole K loop as one chunk.
+// that are odd and above 2^23).  The K loop is therefore cut into equal
+// chunks of at most 1024, each accumulated afresh in one of two TMEM buffers;
+// epilogue warps convert each finished chunk to int32 (exact) and add it to
+// per-thread int32 registers while the tensor core fills the other buffer.
+// Given bounds on the rows' code norms, a work item whose bounds keep every
+// partial sum below 2^24 (Cauchy-Schwarz) runs its whole K loop as one chunk,
+// and the epilogue keeps the accumulator's FP32 bits (the exact integer).
 //
 // Mainloop: the MMA runs on CTA pairs (tcgen05.mma.cta_group::2, M = 256,
 // N = 256, K = 16).  Each CTA of a pair holds its own 128 rows of A and one
@@ -640,8 +641,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         if (!got) { ok = false; break; }
         tc_fence_after();
         const uint32_t t_base = tmem_base + lane_addr + buf * BN + col_half * 128;
-        // 16 columns per load: with 32, the 128 int32 accumulators and the
-        // load's registers exceed the 168-register budget and spill
+        // 16 columns per load: with 32, the 128 accumulators and the load's
+        // registers exceed the 168-register budget and spill
         if (keep_bits) {
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
