@@ -920,10 +920,21 @@ def main():
     # codes resident).  At the whole-GPU rate the weight kernel measured just
     # now, that work alone takes strips x its time, with perfect overlap and no
     # interference with the MMAs assumed, plus a scales-only pre-pass.
+    # Per tile: one CTA pair (2 SMs) would prepare a work item's 256 weight
+    # rows itself; at the measured per-SM rate of the weight kernel that
+    # takes tile_weight_us, against tile_mma_us of GEMM time per item.
     strips = -(-wl.M // 256)
+    items = strips * -(-wl.N // 256)
+    pairs = min(sm_count // 2, items)
+    tile_weight_us = 1e3 * w_ms * sm_count / wl.N * 256 / 2
+    tile_mma_us = 1e3 * g_ms * pairs / items
     decode_in_gemm = {"m_strips": strips, "redone_weight_work_ms": strips * w_ms,
                       "vs_layer_ms": ms_step,
-                      "note": "lower bound on a decode-inside-GEMM layer from this run's weight-kernel time"}
+                      "tile_weight_us": tile_weight_us, "tile_mma_us": tile_mma_us,
+                      "tile_ratio": tile_weight_us / tile_mma_us,
+                      "note": "lower bound on a decode-inside-GEMM layer from this run's weight-kernel time; "
+                              "tile_ratio: one CTA pair preparing a work item's 256 weight rows at the weight "
+                              "kernel's per-SM rate, over the GEMM's time per work item"}
 
     # end-to-end through the public API with host buffers
     e2e_value = e2e_ms = link = intervals = e2e_runs = None
