@@ -245,3 +245,30 @@ def test_codes_do_not_depend_on_asking_for_bounds(wl):
                           torch.tensor([float(t)], dtype=torch.float32, device=DEV), ww.K, q, s, w_norm=nrm)
         wouts.append((q, s))
     assert torch.equal(wouts[0][0], wouts[1][0]) and torch.equal(wouts[0][1], wouts[1][1])
+
+
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp16", "fp32"])
+def test_bias_and_output_dtypes_identical_with_and_without_norm_bounds(out_dtype):
+    # the one-chunk epilogue (FP32 accumulator bits kept) against the chunked
+    # one (int32 sums converted once), with a per-channel bias, every output type
+    import rotated_w4a8_int8_gb300 as cr
+    wl = small("qkv", 200, 300)
+    x = synth.make_activations(wl)
+    packed, scales, t = synth.make_nvfp4_weight(wl)
+    Kp = oracle.padded_k(wl.K)
+    qw = torch.empty(wl.N, Kp, dtype=torch.float16, device=DEV)
+    sw = torch.empty(wl.N, dtype=torch.float32, device=DEV)
+    nw = torch.empty(wl.N, dtype=torch.float32, device=DEV)
+    qa = torch.empty(wl.M, Kp, dtype=torch.float16, device=DEV)
+    sa = torch.empty(wl.M, dtype=torch.float32, device=DEV)
+    na = torch.empty(wl.M, dtype=torch.float32, device=DEV)
+    cr.prepare_weight(torch.from_numpy(packed).to(DEV), torch.from_numpy(scales).to(DEV),
+                      torch.tensor([float(t)], dtype=torch.float32, device=DEV), wl.K, qw, sw, w_norm=nw)
+    cr.quant_act(storage_to_dev(x, wl.x_dtype), wl.K, qa, sa, a_norm=na)
+    assert float(na.max()) * float(nw.max()) < LIMIT
+    bias = (torch.randn(wl.N, generator=torch.Generator().manual_seed(9)) * 0.1).to(DEV)
+    y1 = torch.empty(wl.M, wl.N, dtype=TORCH_DT[out_dtype], device=DEV)
+    y2 = torch.empty_like(y1)
+    cr.gemm(qa, sa, qw, sw, y1, bias=bias)
+    cr.gemm(qa, sa, qw, sw, y2, bias=bias, a_norm=na, w_norm=nw)
+    assert torch.equal(y1, y2)
