@@ -79,7 +79,7 @@ constexpr int TMEM_COLS = 512;                   // two 256-column FP32 buffers
 constexpr int NPAIRS = 1;                        // CTA pairs per cluster (2: they share A by multicast)
 constexpr int CLUSTER = 2 * NPAIRS;              // rank = 2 * pair + half
 constexpr int A_BOX_ROWS = NPAIRS == 2 ? BM / 2 : BM;   // rows of A per TMA load (halves when multicast)
-constexpr int GROUP_M2 = 8;                      // tile raster: 8 pair rows (2048 rows) share each B tile
+constexpr int GROUP_M2 = 16;                     // tile raster: 16 pair rows (4096 rows) share each B tile
 // Output staging: each epilogue warp writes its 32 rows x 128 columns as
 // boxes of 32 rows x 64 bytes (64-byte swizzle), OUT_BUFS buffers per warp,
 // and hands every box to a TMA tensor store.
