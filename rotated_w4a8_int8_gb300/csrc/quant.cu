@@ -270,7 +270,7 @@ __device__ __forceinline__ void act_row(const ActRaw<DT, SWIGLU, NBMAX>& cur, in
   }
   // z = x H; the rotated row is z / 16 (exact), so its absmax is amax / 16
   const float hsk = 0.5001f * sqrtf(static_cast<float>(((K + kBlock - 1) / kBlock) * kBlock));
-  const RowQuant rq = SPLIT == 1 ? cta_rowquant<!SWIGLU>(amax, ss, NORM, red, 0.0625f, hsk)
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, ss, NORM, red, 0.0625f, hsk)
                                  : cluster_rowquant(amax, ss, NORM, red, xred, 0.0625f, hsk);
   if (threadIdx.x == 0 && blk0 == 0) {
     scale[row] = rq.s;
@@ -437,7 +437,7 @@ __device__ __forceinline__ void weight_row(const WRaw<NBMAX>& r, int row, int K,
     }
   }
   const float hsk = 0.5001f * sqrtf(static_cast<float>(((K + kBlock - 1) / kBlock) * kBlock));
-  const RowQuant rq = SPLIT == 1 ? cta_rowquant<true>(amax, ss, NORM, red, 1.0f, hsk)
+  const RowQuant rq = SPLIT == 1 ? cta_rowquant(amax, ss, NORM, red, 1.0f, hsk)
                                  : cluster_rowquant(amax, ss, NORM, red, xred, 1.0f, hsk);
   if (threadIdx.x == 0 && blk0 == 0) {
     scale[row] = rq.s;
