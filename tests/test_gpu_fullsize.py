@@ -1,5 +1,6 @@
 """Parity at the workloads' full sizes, through the same three C-ABI calls the
-benchmark times, checked on sampled outputs that the oracle can compute.
+benchmark times (with the code-norm bounds where the benchmark asks for
+them), checked on sampled outputs that the oracle can compute.
 
 Per workload: every weight row's S8 codes and scale against the oracle; a
 sample of token rows (first, last, M-tile boundaries, random) for the
@@ -11,11 +12,11 @@ import numpy as np
 import pytest
 import torch
 
+import bench
 import oracle
 import synth
-from gpu_util import (DEV, assert_codes_match, assert_output_match, assert_scales_match,
-                      codes_to_np, ensure_built, gpu_gemm, gpu_prepare_weight, gpu_quant_act,
-                      storage_to_dev)
+from gpu_util import (DEV, TORCH_DT, assert_codes_match, assert_output_match, assert_scales_match,
+                      codes_to_np, ensure_built, storage_to_dev)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -38,15 +39,26 @@ def test_full_size_layer(name):
     x = synth.make_activations(wl)
     packed, scales, t = synth.make_nvfp4_weight(wl)
 
-    # the layer on the GPU, as timed by the benchmark
+    # the layer on the GPU, as timed by the benchmark: with the code-norm
+    # bounds where the benchmark asks for them
+    use_norms = bench.norms_pay(Kp)
     xd = storage_to_dev(x, wl.x_dtype)
-    qw, sw = gpu_prepare_weight(packed, scales, t, wl.K)
-    qa, sa = gpu_quant_act(None, wl.x_dtype, wl.K, wl.swiglu, xdev=xd)
-    y = gpu_gemm(qa, sa, qw, sw, wl.out_dtype, Kp)
+    qw = torch.empty(wl.N, Kp, dtype=torch.float16, device=DEV)
+    sw = torch.empty(wl.N, dtype=torch.float32, device=DEV)
+    qa = torch.empty(wl.M, Kp, dtype=torch.float16, device=DEV)
+    sa = torch.empty(wl.M, dtype=torch.float32, device=DEV)
+    nw = torch.empty(wl.N, dtype=torch.float32, device=DEV) if use_norms else None
+    na = torch.empty(wl.M, dtype=torch.float32, device=DEV) if use_norms else None
+    cr.prepare_weight(torch.from_numpy(packed).to(DEV), torch.from_numpy(scales).to(DEV),
+                      torch.tensor([float(t)], dtype=torch.float32, device=DEV), wl.K, qw, sw, w_norm=nw)
+    cr.quant_act(xd, wl.K, qa, sa, swiglu=wl.swiglu, a_norm=na)
+    y = torch.empty(wl.M, wl.N, dtype=TORCH_DT[wl.out_dtype], device=DEV)
+    cr.gemm(qa, sa, qw, sw, y, K_p=Kp, a_norm=na, w_norm=nw)
     rows = sample_rows(wl.M, wl.seed)
     rows_t = torch.from_numpy(rows).to(DEV)
     acc = torch.empty(len(rows), wl.N, dtype=torch.int32, device=DEV)
-    cr.gemm_i32(qa.index_select(0, rows_t).contiguous(), qw, acc, K_p=Kp)
+    na_s = na.index_select(0, rows_t).contiguous() if use_norms else None
+    cr.gemm_i32(qa.index_select(0, rows_t).contiguous(), qw, acc, K_p=Kp, a_norm=na_s, w_norm=nw)
     torch.cuda.synchronize()
     assert cr.device_error() == 0
     g_qw = codes_to_np(qw, Kp)
@@ -55,6 +67,11 @@ def test_full_size_layer(name):
     g_sa = sa.cpu().numpy()[rows]
     g_y = y.index_select(0, rows_t).float().cpu().numpy().astype(np.float64)
     g_acc = acc.cpu().numpy().astype(np.int64)
+    if use_norms:
+        # the bounds hold: every weight row, the sampled token rows
+        for q, b in ((g_qw, nw.cpu().numpy()), (g_qa, na_s.cpu().numpy())):
+            true = np.sqrt(np.sum(q.astype(np.float64) ** 2, axis=1))
+            assert np.all(b.astype(np.float64) >= true)
     del xd, qa, qw, y, acc
     torch.cuda.empty_cache()
 
