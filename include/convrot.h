@@ -227,10 +227,13 @@ int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const float* a_norm,
  * operand tiles runs out (after about two seconds).  The kernel then records
  * the failure, drains and returns; acc is left incomplete.  Afterwards
  * convrot_device_error reports CONVROT_ERR_DEVICE_TIMEOUT with a nonzero
- * code, and the CUDA context stays usable.  Returns the launch status.
+ * code, and the CUDA context stays usable.  With norm bounds (as for
+ * convrot_gemm_i32) and K_p > 1024, the warp that hands chunk counts to the
+ * MMA issuer runs as well and must leave its waits on the abort too.  Returns
+ * the launch status.
  */
-int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq,
-                                  const void* w_q, int64_t ld_wq,
+int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, const float* a_norm,
+                                  const void* w_q, int64_t ld_wq, const float* w_norm,
                                   int M, int N, int K_p,
                                   int32_t* acc, int64_t ld_acc, cudaStream_t stream);
 

@@ -60,7 +60,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.convrot_gemm_i32.restype = i32
     lib.convrot_widen_codes.argtypes = [vp, i64, i32, i32, vp, i64, vp]
     lib.convrot_widen_codes.restype = i32
-    lib.convrot_gemm_timeout_selftest.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp, i64, vp]
+    lib.convrot_gemm_timeout_selftest.argtypes = [vp, i64, vp, vp, i64, vp, i32, i32, i32, vp, i64, vp]
     lib.convrot_gemm_timeout_selftest.restype = i32
     lib.convrot_int8_mma_probe.argtypes = [i32, i32, vp, vp]
     lib.convrot_int8_mma_probe.restype = i32
@@ -170,12 +170,12 @@ def widen_codes(src, dst, cols: int | None = None, stream=None) -> None:
         _ptr(src), _ld(src), rows, int(cols), _ptr(dst), _ld(dst), _stream(stream)))
 
 
-def gemm_timeout_selftest(a_q, w_q, acc, K_p: int | None = None, stream=None) -> None:
+def gemm_timeout_selftest(a_q, w_q, acc, K_p: int | None = None, a_norm=None, w_norm=None, stream=None) -> None:
     """convrot_gemm_timeout_selftest: the GEMM with its producer off (a wait runs out)."""
     M, N = a_q.shape[0], w_q.shape[0]
     K_p = a_q.shape[1] if K_p is None else K_p
     _check("convrot_gemm_timeout_selftest", load_library().convrot_gemm_timeout_selftest(
-        _ptr(a_q), _ld(a_q), _ptr(w_q), _ld(w_q), M, N, int(K_p), _ptr(acc),
+        _ptr(a_q), _ld(a_q), _ptr(a_norm), _ptr(w_q), _ld(w_q), _ptr(w_norm), M, N, int(K_p), _ptr(acc),
         _ld(acc), _stream(stream)))
 
 

@@ -999,14 +999,15 @@ extern "C" int convrot_gemm_i32(const void* a_q, int64_t ld_aq, const float* a_n
              stream);
 }
 
-extern "C" int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, const void* w_q,
-                                             int64_t ld_wq, int M, int N, int K_p, int32_t* acc,
-                                             int64_t ld_acc, cudaStream_t stream) {
+extern "C" int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, const float* a_norm, const void* w_q,
+                                             int64_t ld_wq, const float* w_norm, int M, int N, int K_p,
+                                             int32_t* acc, int64_t ld_acc, cudaStream_t stream) {
   int st = validate_operands(a_q, ld_aq, w_q, ld_wq, M, N, K_p);
   if (st != CONVROT_OK) return st;
   if (M == 0 || N == 0 || !acc || ld_acc < N) return CONVROT_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(acc) % 4) return CONVROT_ERR_MISALIGNED;
-  return run(-1, a_q, ld_aq, nullptr, nullptr, w_q, ld_wq, nullptr, nullptr, nullptr, M, N, K_p, acc, ld_acc, 4,
+  if ((st = check_norms(a_norm, w_norm)) != CONVROT_OK) return st;
+  return run(-1, a_q, ld_aq, nullptr, a_norm, w_q, ld_wq, nullptr, w_norm, nullptr, M, N, K_p, acc, ld_acc, 4,
              stream, 1);
 }
 
