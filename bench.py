@@ -410,8 +410,10 @@ class E2EPipeline:
             while not t1.query():
                 pass
         t1.synchronize()
-        # intervals between consecutive steps' output completions
+        # intervals between consecutive steps' output completions, and the
+        # pipeline's fill: the start to the first step's output
         self.step_ms = [marks[i - 1].elapsed_time(marks[i]) for i in range(1, len(marks))]
+        self.first_ms = t0.elapsed_time(marks[0]) if marks else None
         return t0.elapsed_time(t1)
 
 
@@ -496,14 +498,14 @@ def time_e2e(layer: Layer, steps: int, warmup: int, world: int, runs: int = 3):
         ms = pipe.run(steps)
         torch.cuda.synchronize()
         barrier(world)
-        results.append((ms, list(pipe.step_ms)))
+        results.append((ms, list(pipe.step_ms), pipe.first_ms))
     order = sorted(range(runs), key=lambda r: results[r][0])
-    ms, step_ms = results[order[runs // 2]]
+    ms, step_ms, first_ms = results[order[runs // 2]]
     iv = sorted(step_ms)
     intervals = None
     if iv:
         intervals = {"min": iv[0], "median": iv[len(iv) // 2], "max": iv[-1],
-                     "first": step_ms[0], "last": step_ms[-1]}
+                     "first": step_ms[0], "last": step_ms[-1], "to_first_output": first_ms}
     runs_ms_per_step = [r[0] / steps for r in results]
     return ms, pipe.in_bytes, pipe.out_bytes, link, intervals, runs_ms_per_step
 
@@ -829,7 +831,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qkv", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    # 50 pipelined layers per timed run, as a DiT of 50 blocks runs them back to back; the
+    # pipeline's fill (to the first output) is reported beside the per-step intervals
+    ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--overlap", type=int, default=0,
                     help="1: the headline layer time runs the weight preparation on a second stream beside the "
                          "activation quantisation (per-kernel times come from a serial pass); 0: serial only")
