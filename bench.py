@@ -633,6 +633,50 @@ def time_controls(wl: synth.Workload, dev, world, flush, warmup, steps=20):
     return out
 
 
+def time_decode_probe(layer: "Layer", strips: int, g_ms: float, warmup: int, reps: int = 5):
+    """The producer of a decode-inside-GEMM measured: convrot_decode_gemm_probe
+    runs, one CTA per SM, every work unit of this layer's GEMM (each 256-token
+    strip x each 128-row weight half) and builds that unit's FP16 weight codes
+    from the NVFP4 bytes into the GEMM's swizzled shared-memory B layout, with
+    a consumer that releases each stage at once (an MMA that takes no time).
+    A fused GEMM can be no faster than its producer, so `ratio` (the best
+    producer time over the layer GEMM's time in this run) bounds what decode
+    inside the GEMM would cost; `unit_us` is one SM's time per unit, against
+    the GEMM's time per 256 x 256 work item on its CTA pair (tile_mma_us).
+    The NVFP4 weight stays in L2 (no flush), which favours the probe.  8 and
+    16 producer warps are timed; the best is kept."""
+    import torch
+    cr = layer.cr
+    status = torch.zeros(1, dtype=torch.int32, device=layer.x.device)
+    out = {}
+    for pw in (8, 16):
+        def run():
+            cr.decode_gemm_probe(layer.p, layer.s, layer.t, layer.sw, layer.wl.K, strips, pw, status)
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise SystemExit(f"decode-GEMM probe: a wait ran out (code {int(status.item())})")
+        ts = []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            run()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        out[f"pw{pw}_ms"] = statistics.median(ts)
+    best = min(out["pw8_ms"], out["pw16_ms"])
+    sms = torch.cuda.get_device_properties(layer.x.device).multi_processor_count
+    units = strips * -(-layer.wl.N // 128)
+    out.update({"ms": best, "units": units, "unit_us": 1e3 * best * min(sms, units) / units,
+                "gemm_ms": g_ms, "ratio": best / g_ms,
+                "note": "producer of a decode-inside-GEMM alone over this layer's GEMM schedule, "
+                        "an instant consumer; a fused GEMM is no faster than this (plus a scales-only pass)"})
+    return out
+
+
 def time_library_controls(layer: "Layer", flush, warmup, steps=20):
     """Library controls on the layer's own operands, timed the way the layer's
     GEMM is (L2 flushed before every call, CUDA events on the launching
@@ -850,6 +894,8 @@ def main():
                     help="seconds of back-to-back layers for the sustained-clock leg (0 to skip)")
     ap.add_argument("--library", type=int, default=1,
                     help="also time the cuBLAS FP16 and cuBLASLt INT8 controls on the GEMM's shape (0 to skip)")
+    ap.add_argument("--decode-probe", type=int, default=1,
+                    help="also time the producer of a decode-inside-GEMM over the layer's schedule (0 to skip)")
     ap.add_argument("--rows", type=int, default=0,
                     help="truncate M to this many tokens (small profiling case; not a bench line)")
     args = ap.parse_args()
@@ -939,6 +985,8 @@ def main():
                       "note": "lower bound on a decode-inside-GEMM layer from this run's weight-kernel time; "
                               "tile_ratio: one CTA pair preparing a work item's 256 weight rows at the weight "
                               "kernel's per-SM rate, over the GEMM's time per work item"}
+    if args.decode_probe:
+        decode_in_gemm["producer_probe"] = time_decode_probe(layer, strips, g_ms, args.warmup)
 
     # end-to-end through the public API with host buffers
     e2e_value = e2e_ms = link = intervals = e2e_runs = None

@@ -250,6 +250,35 @@ int convrot_gemm_timeout_selftest(const void* a_q, int64_t ld_aq, const float* a
 int convrot_int8_mma_probe(int blocks, int iters, int32_t* out, cudaStream_t stream);
 
 /*
+ * Measurement aid, not part of the layer: the producer side of a GEMM that
+ * would decode, rotate and quantise the NVFP4 weight inside the GEMM.  The
+ * pages run the weight work beside the GEMM instead (ComfyUI Turing Utils
+ * page, node list, the ConvRot loaders' NVFP4 entry); this measures the
+ * fused form.  One CTA per SM runs the m_strips * ceil(N/128) work units of a
+ * GEMM over m_strips strips of 256 tokens.  For unit u, producer_warps (8 or
+ * 16) warps build the FP16 codes of weight rows 128 * (u % ceil(N/128)) +
+ * [0, 128) over the padded K, one 256-column rotation block at a time, in the
+ * tensor core's swizzled shared-memory layout (two 64 KiB stages), and one
+ * consumer warp releases each stage as soon as it is full.  A fused GEMM is
+ * no faster than this producer.
+ *   w_fp4, w_sf, w_tensor_scale, N, K   as for convrot_prepare_weight.
+ *   w_scale  [N] FP32 row scales that convrot_prepare_weight wrote for this
+ *            weight (a fused layer needs a scales-only pass first).
+ *   dump     optional (NULL: none), device FP16 [128][ld_dump], ld_dump >=
+ *            K_p and even, 4-byte aligned: receives the codes of unit
+ *            dump_unit (rows past N as zeros).  They equal rows
+ *            128 * (dump_unit % ceil(N/128)) + [0, 128) of
+ *            convrot_prepare_weight's FP16 codes.
+ *   status   device int32, set to 0 by the call; the kernel writes a nonzero
+ *            code there if a wait runs out (about two seconds).
+ * Returns the launch status.
+ */
+int convrot_decode_gemm_probe(const uint8_t* w_fp4, const uint8_t* w_sf, const float* w_tensor_scale,
+                              const float* w_scale, int N, int K, int m_strips, int producer_warps,
+                              void* dump, int64_t ld_dump, int dump_unit, int32_t* status,
+                              cudaStream_t stream);
+
+/*
  * Text of the last CUDA error that made a call of this library return
  * CONVROT_ERR_CUDA in the calling thread, naming the failing CUDA call
  * ("" if none).  The string is owned by the library and stays valid until

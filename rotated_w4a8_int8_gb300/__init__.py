@@ -14,7 +14,8 @@ import os
 
 __all__ = [
     "load_library", "padded_k", "status_string", "last_error", "prepare_weight", "quant_act", "gemm",
-    "gemm_i32", "widen_codes", "gemm_timeout_selftest", "int8_mma_probe", "device_error", "ConvRotError", "BF16", "FP16",
+    "gemm_i32", "widen_codes", "gemm_timeout_selftest", "int8_mma_probe", "decode_gemm_probe",
+    "device_error", "ConvRotError", "BF16", "FP16",
     "FP32", "CODES_S8",
     "CODES_F16", "LIB_PATH", "EXPORTS",
 ]
@@ -24,7 +25,8 @@ BF16, FP16, FP32 = 0, 1, 2
 CODES_S8, CODES_F16 = 0, 1
 EXPORTS = ("convrot_padded_k", "convrot_status_string", "convrot_prepare_weight",
            "convrot_quant_act", "convrot_gemm", "convrot_gemm_i32", "convrot_device_error",
-           "convrot_last_error", "convrot_gemm_timeout_selftest", "convrot_widen_codes", "convrot_int8_mma_probe")
+           "convrot_last_error", "convrot_gemm_timeout_selftest", "convrot_widen_codes", "convrot_int8_mma_probe",
+           "convrot_decode_gemm_probe")
 
 _lib = None
 
@@ -64,6 +66,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.convrot_gemm_timeout_selftest.restype = i32
     lib.convrot_int8_mma_probe.argtypes = [i32, i32, vp, vp]
     lib.convrot_int8_mma_probe.restype = i32
+    lib.convrot_decode_gemm_probe.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, i64, i32, vp, vp]
+    lib.convrot_decode_gemm_probe.restype = i32
     lib.convrot_last_error.argtypes = []
     lib.convrot_last_error.restype = ctypes.c_char_p
     lib.convrot_device_error.argtypes = [vp, ctypes.POINTER(i32)]
@@ -183,6 +187,19 @@ def int8_mma_probe(blocks: int, iters: int, out, stream=None) -> None:
     """convrot_int8_mma_probe: out int32 [blocks * 4]; each entry becomes 8 * 32 * iters."""
     _check("convrot_int8_mma_probe", load_library().convrot_int8_mma_probe(
         int(blocks), int(iters), _ptr(out), _stream(stream)))
+
+
+def decode_gemm_probe(w_fp4, w_sf, w_tensor_scale, w_scale, K: int, m_strips: int, producer_warps: int, status,
+                      dump=None, dump_unit: int = 0, stream=None) -> None:
+    """convrot_decode_gemm_probe: the producer of a decode-inside-GEMM over m_strips token strips.
+
+    status: int32 [1] (device); dump: optional FP16 [128, >= K_p] receiving unit dump_unit's codes.
+    """
+    N = w_fp4.shape[0]
+    _check("convrot_decode_gemm_probe", load_library().convrot_decode_gemm_probe(
+        _ptr(w_fp4), _ptr(w_sf), _ptr(w_tensor_scale), _ptr(w_scale), N, int(K), int(m_strips),
+        int(producer_warps), _ptr(dump), _ld(dump) if dump is not None else 0, int(dump_unit), _ptr(status),
+        _stream(stream)))
 
 
 def device_error(stream=None) -> int:

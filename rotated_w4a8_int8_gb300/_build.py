@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libconvrot.so")
 # with the kernels that write code-norm bounds
 SOURCES = [("api.cu", "api", []), ("quant.cu", "quant", []),
            ("quant.cu", "quant_norm", ["-DCONVROT_QUANT_NORM=1"]), ("gemm.cu", "gemm", []),
-           ("int8_probe.cu", "int8_probe", [])]
+           ("int8_probe.cu", "int8_probe", []), ("decode_gemm_probe.cu", "decode_gemm_probe", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -141,3 +141,30 @@ def test_int8_probe_rejects_bad_arguments(lib):
     assert f(4, (1 << 22) + 1, P, 0) == 1           # the per-warp sum would overflow int32
     assert f(4, 10, None, 0) == 1
     assert f(4, 10, P + 2, 0) == 2                  # int32 output misaligned
+
+
+def test_decode_gemm_probe_rejects_bad_arguments(lib):
+    f = lib.convrot_decode_gemm_probe
+    P = 1 << 20                                     # aligned fake device addresses: no call reaches the GPU
+    ok = dict(w=P, sf=P, t=P, s=P, N=256, K=5376, ms=2, pw=16, dump=None, ld=0, unit=0, st=P)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["w"], a["sf"], a["t"], a["s"], a["N"], a["K"], a["ms"], a["pw"], a["dump"], a["ld"],
+                 a["unit"], a["st"], None)
+    assert call(N=0) == 1
+    assert call(K=0) == 1
+    assert call(ms=0) == 1
+    assert call(pw=4) == 3                          # 8 or 16 producer warps
+    assert call(K=65537) == 3                       # K_p beyond the limit
+    assert call(w=None) == 1
+    assert call(s=None) == 1
+    assert call(st=None) == 1
+    assert call(w=P + 4) == 2
+    assert call(s=P + 2) == 2
+    assert call(st=P + 2) == 2
+    assert call(dump=P, ld=5120) == 1               # ld_dump below K_p
+    assert call(dump=P, ld=5376, unit=4) == 1       # 2 strips x 2 halves: units 0..3
+    assert call(dump=P, ld=5376, unit=-1) == 1
+    assert call(dump=P + 2, ld=5376) == 2
+    assert call(dump=P, ld=5378 + 1) == 2            # odd pitch
