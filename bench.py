@@ -46,7 +46,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic (read + write bytes) of one full-size QKV GEMM launch, from an ncu capture of
 # this kernel; valid only while code_sha16(gemm.cu) equals this (the hash ignores comments;
 # otherwise the bench line reports traffic as null).
-GEMM_TRAFFIC = {"sha256_16": "83f188524591c2c6", "bytes": 2581869824 + 934568704}
+GEMM_TRAFFIC = {"sha256_16": "821fc3350e166564", "bytes": 2865981184 + 924844032}
 
 
 def code_sha16(path: str) -> str:

@@ -117,14 +117,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
+// completes (or kSuspendNs pass) instead of polling.  Polling waits (the
+// epilogue warps for a finished accumulator, the producer for a free stage,
+// the issuer for a full one) cost the QKV GEMM 5% (2.282 -> 2.166 ms, same
+// box, alternating order); a 1 us hint measured the same as 20 us.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -180,17 +186,17 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
   return r;
 }
 
-// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
-// another's), with the default CTA-scope release: the epilogue uses it to
-// hand a drained TMEM buffer back to the pair's MMA issuer, and the tensor
-// memory reads it orders are fenced by tcgen05.fence::before_thread_sync (a
-// cluster-scope release here made every arrive a cluster-wide memory fence).
 // Arrive on a barrier of this CTA (release at CTA scope: writes before it are
 // seen by a thread whose wait completes the phase).
 __device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
+// another's), with the default CTA-scope release: the epilogue uses it to
+// hand a drained TMEM buffer back to the pair's MMA issuer, and the tensor
+// memory reads it orders are fenced by tcgen05.fence::before_thread_sync (a
+// cluster-scope release here made every arrive a cluster-wide memory fence).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
