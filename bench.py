@@ -73,8 +73,10 @@ def load_peaks():
 # ---------------------------------------------------------------- workload sizes
 def norms_pay(Kp: int) -> bool:
     """Whether the layer asks the quantisation kernels for code-norm bounds.
-    They cost the kernels a sum of squares (2-5% of their time) and let the
-    GEMM run a tile as one FP32 chunk when max bound(A) x max bound(B) < 2^24.
+    They cost the kernels a sum of squares (about 10 us each at QKV) and let
+    the GEMM run a tile as one FP32 chunk when max bound(A) x max bound(B) <
+    2^24, which saves it about as much (the drains of the exact chunks cost
+    the QKV GEMM about 1%).
     Rotated rows of ordinary data have codes with an RMS of about 30-36, so a
     bound near 33 sqrt(K_p): the product stays below 2^24 up to K_p of about
     8192-13000 (QKV, K_p = 5376: about 2300 each) and not at K_p = 14336

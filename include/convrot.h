@@ -138,8 +138,10 @@ int convrot_prepare_weight(const uint8_t* w_fp4, const uint8_t* w_sf,
  *   a_norm  NULL, or [M] FP32 (4-byte aligned): an upper bound on the
  *           Euclidean norm of each row's codes, for convrot_gemm.  Asking
  *           for it adds a sum of squares to the kernel (a few percent of its
- *           time); it pays where the bounds let the GEMM skip its chunk
- *           drains, i.e. for ordinary rotated data up to K_p of about 8192.
+ *           time); the bounds let the GEMM run a tile as one chunk, which
+ *           for ordinary rotated data holds up to K_p of about 8192 (at
+ *           K_p = 5376 the drains it skips cost about as much, 1% of the
+ *           GEMM).
  *           The codes and scales are the same either way.
  *
  * Quantiser as for the weights (FP32 scale, FP32 reciprocal, FP32 product,
