@@ -199,7 +199,8 @@ producer_probe_kernel(const uint8_t* __restrict__ w_fp4, const uint8_t* __restri
         if (b + 1 < nblocks) {                     // next block's raw input, in flight during this one
 #pragma unroll
           for (int r = 0; r < R; ++r)
-            if (valid[r]) load_nvfp4_raw<W16>(prow[r], srow[r], (b + 1) * kBlock + 32 * lane8, K, K_s, w0[r], w1[r], sc[r]);
+            if (valid[r])
+              load_nvfp4_raw<W16>(prow[r], srow[r], (b + 1) * kBlock + 32 * lane8, K, K_s, w0[r], w1[r], sc[r]);
         }
         const uint32_t buf = use & 1u, ph = (use >> 1) & 1u;
         if (!warp_wait(empty0 + 8 * buf, ph ^ 1u, PROBE_WAIT_EMPTY, abort_flag, status)) { ok = false; break; }
