@@ -20,7 +20,10 @@
  *     allocated, freed or retained by the library.
  *   - Work is enqueued on `stream` (0 = legacy default stream) and the call
  *     returns without synchronising.  Outputs are valid once the stream has
- *     reached the work.
+ *     reached the work.  Since the three layer calls only enqueue kernels,
+ *     a caller may capture them into a CUDA graph (after one eager call on
+ *     the device, which sets up per-device launch attributes) and replay it
+ *     on new contents of the same buffers.
  *   - Matrices are row-major.  Leading dimensions (ld_*) count ELEMENTS of
  *     the matrix's own storage type.
  *   - K is the logical reduction width; K_p = convrot_padded_k(K) is K
