@@ -484,7 +484,10 @@ def host_link_gbs(pipe: "E2EPipeline", reps: int = 3):
     return out
 
 
-def time_e2e(layer: Layer, steps: int, warmup: int, world: int, runs: int = 3):
+E2E_RUNS = 5
+
+
+def time_e2e(layer: Layer, steps: int, warmup: int, world: int, runs: int = E2E_RUNS):
     """`runs` timed runs of `steps` pipelined steps; returns the median run's
     time and per-step intervals, and every run's ms per step.  On some boxes a
     single step of a run stalled for tens of milliseconds (its neighbours at
@@ -1094,7 +1097,7 @@ def main():
         "e2e": {"value": e2e_value, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "pipelined": "streams: copy-in, kernels, copy-out split over 2 copy streams",
                 "ms_per_step": e2e_ms / args.e2e_steps if e2e_ms else None,
-                "statistic": "median of 3 timed runs of e2e_steps pipelined steps",
+                "statistic": f"median of {E2E_RUNS} timed runs of e2e_steps pipelined steps",
                 "runs_ms_per_step": e2e_runs,
                 "host_link_gbs": link,
                 # time between consecutive steps' output completions: a slow box shows here
