@@ -876,7 +876,9 @@ def bench_config(wl: synth.Workload, overlap: int) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20,
+                    help="timed layers (a short run: the unthrottled regime the burst peak is measured in; "
+                         "the sustained leg covers the power-capped one)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qkv", choices=sorted(synth.WORKLOADS))
