@@ -256,9 +256,10 @@ __device__ __forceinline__ RowQuant cta_rowquant(float local, float ss, bool wit
 // this CTA's per-warp maxima and sums of squares and publishes them in
 // xred[0], xred[1]; after a cluster barrier it reads the peer's, computes s
 // and r and leaves them in xred[2], xred[3] for the CTA; thread 0 leaves the
-// norm bound in xred[4] after the last barrier.  Every thread of both CTAs must call it and then call
-// cluster_exit_wait() once before the CTA exits (the peer may read xred
-// until then).  xred = red + 16; the per-warp sums use red[24, 40).
+// norm bound in xred[4] after the last barrier.  Every thread of both CTAs
+// must call it and then call cluster_exit_wait() once before the CTA exits
+// (the peer may read xred until then).  xred = red + 16; the per-warp sums
+// use red[24, 40).
 __device__ __forceinline__ RowQuant cluster_rowquant(float local, float ss, bool with_ss, float* red, float* xred,
                                                      float pre, float half_sqrt_kp) {
   local = warp_max_nonneg(local);
